@@ -1,0 +1,859 @@
+// Host engine of kvx: validation, chunk planning, the pinned staging ring,
+// reusable descriptor buffers, the launch table, device status, the C ABI.
+//
+// The path of one kvx_copy_batch (PegaFlow issue #408, §Summary: one
+// descriptor upload and one copy-kernel launch instead of one memcpy per
+// fragment):
+//   1. validate the descriptors (arrays, direction, 8-byte alignment, address
+//      overflow, chunk capacity; overlap and address kinds at higher levels);
+//   2. cut every descriptor into chunks of at most 16 KiB and pack the 32-byte
+//      records into a pinned staging slot (the reused pinned descriptor
+//      buffers of the vLLM PR #42212 report, §实现拆解 item 3 and §评论区精华:
+//      an unpinned buffer makes the "asynchronous" upload synchronous);
+//   3. one cudaMemcpyAsync of the table to the slot's device buffer;
+//   4. one launch of the persistent copy kernel with min(cta_budget, work)
+//      CTAs;
+//   5. record the slot's event and return: enqueue-only (PegaFlow issue #408,
+//      follow-up §2).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cerrno>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "kvx_internal.h"
+
+using kvx::Launch;
+
+// ---------------------------------------------------------------------------
+// error reporting
+// ---------------------------------------------------------------------------
+namespace {
+
+thread_local std::string t_err;
+
+kvx_status fail(kvx_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return s;
+}
+
+kvx_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(KVX_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define KVX_CUDA_TRY(call)                         \
+    do {                                           \
+        cudaError_t e_ = (call);                   \
+        if (e_ != cudaSuccess)                     \
+            return cuda_fail(e_, #call);           \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// environment settings (an unknown value is an error on every call, so that a
+// typo cannot silently select a default: FreeToken issue #751, §What we
+// changed, on its own switch)
+// ---------------------------------------------------------------------------
+struct EnvSettings {
+    int validate = 0;
+    int variant = KVX_VARIANT_AUTO;
+    int cta_budget = 0;
+    std::string error;
+};
+
+const EnvSettings &env()
+{
+    static EnvSettings s = [] {
+        EnvSettings e;
+        if (const char *v = getenv("KVX_VALIDATE")) {
+            if (!strcmp(v, "0") || !strcmp(v, "1") || !strcmp(v, "2"))
+                e.validate = v[0] - '0';
+            else
+                e.error = std::string("KVX_VALIDATE=") + v + " is not 0, 1 or 2";
+        }
+        if (const char *v = getenv("KVX_VARIANT")) {
+            if (!strcmp(v, "auto"))
+                e.variant = KVX_VARIANT_AUTO;
+            else if (!strcmp(v, "ldg"))
+                e.variant = KVX_VARIANT_LDG;
+            else if (!strcmp(v, "bulk"))
+                e.variant = KVX_VARIANT_BULK;
+            else
+                e.error = std::string("KVX_VARIANT=") + v + " is not auto, ldg or bulk";
+        }
+        if (const char *v = getenv("KVX_CTA_BUDGET")) {
+            char *end = nullptr;
+            errno = 0;
+            long b = strtol(v, &end, 10);
+            if (errno || end == v || *end || b < 0 || b > (1 << 20))
+                e.error = std::string("KVX_CTA_BUDGET=") + v + " is not an integer in [0, 2^20]";
+            else
+                e.cta_budget = (int)b;
+        }
+        return e;
+    }();
+    return s;
+}
+
+std::atomic<int> g_validate_level{-1};
+
+int validate_level()
+{
+    int v = g_validate_level.load(std::memory_order_relaxed);
+    return v >= 0 ? v : env().validate;
+}
+
+kvx_status check_env()
+{
+    if (!env().error.empty())
+        return fail(KVX_ERR_INVALID_ARG, "%s", env().error.c_str());
+    return KVX_OK;
+}
+
+// ---------------------------------------------------------------------------
+// validation and chunk planning (host only)
+// ---------------------------------------------------------------------------
+inline uint64_t chunks_of(uint64_t size)
+{
+    return (size + KVX_CHUNK_BYTES - 1) / KVX_CHUNK_BYTES;
+}
+
+struct Range {
+    uint64_t lo, hi;
+    bool operator<(const Range &o) const { return lo < o.lo; }
+};
+
+kvx_status check_overlap(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n)
+{
+    std::vector<Range> d;
+    d.reserve(n);
+    for (size_t i = 0; i < n; ++i)
+        if (sizes[i])
+            d.push_back({dst[i], dst[i] + sizes[i]});
+    std::sort(d.begin(), d.end());
+    for (size_t k = 1; k < d.size(); ++k)
+        if (d[k].lo < d[k - 1].hi)
+            return fail(KVX_ERR_OVERLAP, "destination ranges [0x%llx, 0x%llx) and [0x%llx, 0x%llx) overlap",
+                        (unsigned long long)d[k - 1].lo, (unsigned long long)d[k - 1].hi,
+                        (unsigned long long)d[k].lo, (unsigned long long)d[k].hi);
+    // Destination ranges are now disjoint and sorted by start, hence by end:
+    // the last one starting before a source range ends is the only candidate.
+    for (size_t i = 0; i < n; ++i) {
+        if (!sizes[i])
+            continue;
+        const Range s{src[i], src[i] + sizes[i]};
+        auto it = std::lower_bound(d.begin(), d.end(), Range{s.hi, 0});
+        if (it != d.begin() && std::prev(it)->hi > s.lo)
+            return fail(KVX_ERR_OVERLAP, "descriptor %zu: source range overlaps a destination range", i);
+    }
+    return KVX_OK;
+}
+
+bool kind_ok(uint64_t addr, bool want_host)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, reinterpret_cast<const void *>(addr)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged)
+        return true;
+    return want_host ? (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr)
+                     : a.type == cudaMemoryTypeDevice;
+}
+
+kvx_status check_kinds(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n, int dir)
+{
+    const bool src_host = dir == KVX_H2D, dst_host = dir == KVX_D2H;
+    for (size_t i = 0; i < n; ++i) {
+        if (!sizes[i])
+            continue;
+        if (!kind_ok(src[i], src_host) || !kind_ok(src[i] + sizes[i] - 1, src_host))
+            return fail(KVX_ERR_NOT_MAPPED, "descriptor %zu: source 0x%llx is not %s memory", i,
+                        (unsigned long long)src[i], src_host ? "mapped pinned host" : "device");
+        if (!kind_ok(dst[i], dst_host) || !kind_ok(dst[i] + sizes[i] - 1, dst_host))
+            return fail(KVX_ERR_NOT_MAPPED, "descriptor %zu: destination 0x%llx is not %s memory", i,
+                        (unsigned long long)dst[i], dst_host ? "mapped pinned host" : "device");
+    }
+    return KVX_OK;
+}
+
+// Validate and count chunks and payload bytes.
+kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                    int dir, int level, uint64_t *n_chunks, uint64_t *payload)
+{
+    if (dir < KVX_H2D || dir > KVX_D2D)
+        return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
+    if (level < 0 || level > 2)
+        return fail(KVX_ERR_INVALID_ARG, "validation level %d is not 0, 1 or 2", level);
+    uint64_t chunks = 0, bytes = 0;
+    if (n) {
+        if (!src || !dst || !sizes)
+            return fail(KVX_ERR_INVALID_ARG, "null descriptor array with n = %zu", n);
+        for (size_t i = 0; i < n; ++i) {
+            const uint64_t z = sizes[i];
+            if (!z)
+                continue;
+            const uint64_t s = src[i], d = dst[i];
+            if (!s || !d)
+                return fail(KVX_ERR_INVALID_ARG, "descriptor %zu: null address", i);
+            if ((s | d | z) & 7u)
+                return fail(KVX_ERR_ALIGN,
+                            "descriptor %zu: src 0x%llx, dst 0x%llx, size %llu not all multiples of 8", i,
+                            (unsigned long long)s, (unsigned long long)d, (unsigned long long)z);
+            if (s + z < s || d + z < d)
+                return fail(KVX_ERR_INVALID_ARG, "descriptor %zu: range wraps the address space", i);
+            chunks += chunks_of(z);
+            bytes += z;
+            if (chunks > KVX_MAX_CHUNKS)
+                return fail(KVX_ERR_CAPACITY, "batch needs more than KVX_MAX_CHUNKS (%u) chunks",
+                            KVX_MAX_CHUNKS);
+        }
+    }
+    if (level >= 1 && n) {
+        kvx_status st = check_overlap(src, dst, sizes, n);
+        if (st != KVX_OK)
+            return st;
+    }
+    if (level >= 2 && n) {
+        kvx_status st = check_kinds(src, dst, sizes, n, dir);
+        if (st != KVX_OK)
+            return st;
+    }
+    if (n_chunks)
+        *n_chunks = chunks;
+    if (payload)
+        *payload = bytes;
+    return KVX_OK;
+}
+
+// Pack the chunk records of a validated batch. Chunk k of a descriptor covers
+// bytes [k * 16 KiB, min((k + 1) * 16 KiB, size)).
+size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n, kvx_chunk *out)
+{
+    size_t m = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const uint64_t z = sizes[i];
+        for (uint64_t o = 0; o < z; o += KVX_CHUNK_BYTES) {
+            kvx_chunk &c = out[m++];
+            c.src = src[i] + o;
+            c.dst = dst[i] + o;
+            c.len = (uint32_t)std::min<uint64_t>(KVX_CHUNK_BYTES, z - o);
+            c.desc = (uint32_t)i;
+            c.reserved = 0;
+        }
+    }
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// launch table
+// ---------------------------------------------------------------------------
+// Rows by direction and mean chunk size. The host-link rows target bytes in
+// flight rather than threads (FreeToken issue #751, §Measured impact and
+// §Proposal: the optimum follows bytes in flight); the D2D row fills the GPU.
+struct TableRow {
+    int dir;
+    uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
+    kvx_launch cfg;
+};
+
+const TableRow kTable[] = {
+    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
+    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 304, 256, 8, 3, 0}},
+};
+
+kvx_launch table_launch(int dir, uint64_t mean_chunk)
+{
+    for (const TableRow &r : kTable)
+        if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
+            return r.cfg;
+    return kTable[0].cfg;
+}
+
+// Merge explicit settings over env over table and check them.
+kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch *out)
+{
+    kvx_launch t = table_launch(dir, mean_chunk);
+    const EnvSettings &e = env();
+    int variant = (want && want->variant) ? want->variant : (e.variant ? e.variant : t.variant);
+    int budget = (want && want->cta_budget) ? want->cta_budget : (e.cta_budget ? e.cta_budget : t.cta_budget);
+    int threads = (want && want->threads) ? want->threads : t.threads;
+    int unroll = (want && want->unroll) ? want->unroll : t.unroll;
+    int stages = (want && want->stages) ? want->stages : t.stages;
+    int policy = (want && want->store_policy) ? want->store_policy : t.store_policy;
+    if (want) {
+        if (want->variant < 0 || want->variant > KVX_VARIANT_BULK)
+            return fail(KVX_ERR_INVALID_ARG, "variant %d is not AUTO, LDG or BULK", want->variant);
+        if (want->cta_budget < 0)
+            return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", want->cta_budget);
+        if (want->threads && want->threads != 128 && want->threads != 256 && want->threads != 512)
+            return fail(KVX_ERR_INVALID_ARG, "threads %d is not 128, 256 or 512", want->threads);
+        if (want->unroll && want->unroll != 2 && want->unroll != 4 && want->unroll != 8)
+            return fail(KVX_ERR_INVALID_ARG, "unroll %d is not 2, 4 or 8", want->unroll);
+        if (want->stages && (want->stages < 2 || want->stages > 4))
+            return fail(KVX_ERR_INVALID_ARG, "stages %d is not in 2..4", want->stages);
+        if (want->store_policy < 0 || want->store_policy > 2)
+            return fail(KVX_ERR_INVALID_ARG, "store_policy %d is not 0, 1 or 2", want->store_policy);
+    }
+    if (variant == KVX_VARIANT_AUTO)
+        variant = t.variant;
+    out->variant = variant;
+    out->ctas = budget;
+    out->threads = threads;
+    out->unroll = unroll;
+    out->stages = stages;
+    out->store_policy = policy;
+    return KVX_OK;
+}
+
+kvx_status is_capturing(cudaStream_t stream, bool *cap)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    KVX_CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+    *cap = cs != cudaStreamCaptureStatusNone;
+    return KVX_OK;
+}
+
+// ---------------------------------------------------------------------------
+// pinned staging ring (per device)
+// ---------------------------------------------------------------------------
+constexpr int kRingSlots = 8;
+constexpr int kMaxDevices = 64;
+constexpr size_t kMinSlotChunks = 1 << 16;
+
+struct Slot {
+    kvx_chunk *host = nullptr;  // pinned
+    kvx_chunk *dev = nullptr;
+    size_t cap = 0;             // chunks
+    cudaEvent_t done = nullptr;
+    bool recorded = false;
+    bool busy = false;          // held by a caller between acquire and release
+};
+
+struct Ring {
+    std::mutex mu;
+    Slot slots[kRingSlots];
+    unsigned next = 0;
+};
+
+Ring g_rings[kMaxDevices];
+
+kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
+    Ring &r = g_rings[dev];
+    Slot *s = nullptr;
+    {
+        std::lock_guard<std::mutex> g(r.mu);
+        for (int t = 0; t < kRingSlots && !s; ++t) {
+            Slot &c = r.slots[r.next++ % kRingSlots];
+            if (!c.busy)
+                s = &c;
+        }
+        if (!s)
+            return fail(KVX_ERR_CAPACITY, "all %d staging slots are held by concurrent callers", kRingSlots);
+        s->busy = true;
+    }
+    auto release_on_error = [&](kvx_status st) {
+        std::lock_guard<std::mutex> g(r.mu);
+        s->busy = false;
+        return st;
+    };
+    if (!s->done) {
+        cudaError_t e = cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming);
+        if (e != cudaSuccess)
+            return release_on_error(cuda_fail(e, "cudaEventCreateWithFlags"));
+    }
+    if (s->recorded) {  // wait until the copy that last used this slot has finished
+        cudaError_t e = cudaEventSynchronize(s->done);
+        if (e != cudaSuccess)
+            return release_on_error(cuda_fail(e, "cudaEventSynchronize(staging slot)"));
+        s->recorded = false;
+    }
+    if (s->cap < chunks) {
+        size_t cap = std::max(chunks, std::max(kMinSlotChunks, 2 * s->cap));
+        if (cap > KVX_MAX_CHUNKS)
+            cap = std::max<size_t>(chunks, KVX_MAX_CHUNKS);
+        if (s->host)
+            cudaFreeHost(s->host);
+        if (s->dev)
+            cudaFree(s->dev);
+        s->host = nullptr;
+        s->dev = nullptr;
+        s->cap = 0;
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&s->host), cap * sizeof(kvx_chunk),
+                                      cudaHostAllocPortable);
+        if (e != cudaSuccess)
+            return release_on_error(cuda_fail(e, "cudaHostAlloc(staging slot)"));
+        e = cudaMalloc(reinterpret_cast<void **>(&s->dev), cap * sizeof(kvx_chunk));
+        if (e != cudaSuccess) {
+            cudaFreeHost(s->host);
+            s->host = nullptr;
+            return release_on_error(cuda_fail(e, "cudaMalloc(staging slot)"));
+        }
+        s->cap = cap;
+    }
+    *out = s;
+    return KVX_OK;
+}
+
+void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
+{
+    if (record && cudaEventRecord(s->done, stream) == cudaSuccess)
+        s->recorded = true;
+    std::lock_guard<std::mutex> g(g_rings[dev].mu);
+    s->busy = false;
+}
+
+// mapped pinned words for kvx_stream_check
+struct StatusWords {
+    std::mutex mu;
+    unsigned *words = nullptr;
+    unsigned next = 0;
+};
+StatusWords g_status_words[kMaxDevices];
+constexpr unsigned kStatusWords = 1024;
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// descriptor buffers
+// ---------------------------------------------------------------------------
+struct kvx_desc_buf {
+    std::mutex mu;
+    int device = 0;
+    size_t cap = 0;
+    kvx_chunk *dev = nullptr;
+    kvx_chunk *host = nullptr;
+    cudaEvent_t upload_done = nullptr;
+    cudaEvent_t last_use = nullptr;
+    bool upload_recorded = false;
+    bool use_recorded = false;
+    uint32_t n_chunks = 0;
+    uint64_t payload = 0;
+    int dir = KVX_H2D;
+    kvx_launch selected{};
+};
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char *kvx_status_string(int s)
+{
+    switch (s) {
+    case KVX_OK: return "KVX_OK";
+    case KVX_ERR_INVALID_ARG: return "KVX_ERR_INVALID_ARG";
+    case KVX_ERR_ALIGN: return "KVX_ERR_ALIGN";
+    case KVX_ERR_OVERLAP: return "KVX_ERR_OVERLAP";
+    case KVX_ERR_CAPACITY: return "KVX_ERR_CAPACITY";
+    case KVX_ERR_NOT_MAPPED: return "KVX_ERR_NOT_MAPPED";
+    case KVX_ERR_CUDA: return "KVX_ERR_CUDA";
+    case KVX_ERR_TIMEOUT: return "KVX_ERR_TIMEOUT";
+    case KVX_ERR_DEVICE_FAULT: return "KVX_ERR_DEVICE_FAULT";
+    case KVX_ERR_CAPTURE: return "KVX_ERR_CAPTURE";
+    default: return "KVX_ERR_UNKNOWN";
+    }
+}
+
+const char *kvx_last_error(void) { return t_err.c_str(); }
+
+int kvx_version(void) { return KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR; }
+
+kvx_status kvx_set_validate_level(int level)
+{
+    if (level < 0 || level > 2)
+        return fail(KVX_ERR_INVALID_ARG, "validation level %d is not 0, 1 or 2", level);
+    g_validate_level.store(level);
+    return KVX_OK;
+}
+
+int kvx_get_validate_level(void) { return validate_level(); }
+
+kvx_status kvx_validate(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                        int dir, int level)
+{
+    return validate(src, dst, sizes, n, dir, level, nullptr, nullptr);
+}
+
+kvx_status kvx_plan_chunks(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                           kvx_chunk *out, size_t max_out, size_t *n_chunks)
+{
+    uint64_t chunks = 0;
+    kvx_status st = validate(src, dst, sizes, n, KVX_H2D, 0, &chunks, nullptr);
+    if (st != KVX_OK)
+        return st;
+    if (n_chunks)
+        *n_chunks = (size_t)chunks;
+    if (!out)
+        return KVX_OK;
+    if (chunks > max_out)
+        return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, output holds %zu",
+                    (unsigned long long)chunks, max_out);
+    pack(src, dst, sizes, n, out);
+    return KVX_OK;
+}
+
+kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *out)
+{
+    if (dir < KVX_H2D || dir > KVX_D2D)
+        return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
+    if (!out)
+        return fail(KVX_ERR_INVALID_ARG, "null output");
+    *out = table_launch(dir, mean_chunk_bytes);
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                             int dir, const kvx_launch *want, void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    uint64_t chunks = 0, payload = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    if (st != KVX_OK)
+        return st;
+    Launch l;
+    st = resolve(dir, chunks ? payload / chunks : 0, want, &l);
+    if (st != KVX_OK)
+        return st;
+    if (chunks == 0)
+        return KVX_OK;
+    bool cap = false;
+    st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
+    if (cap)
+        return fail(KVX_ERR_CAPTURE,
+                    "kvx_copy_batch writes a host staging slot; capture kvx_copy_uploaded instead");
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    Slot *s = nullptr;
+    st = ring_acquire(dev, (size_t)chunks, &s);
+    if (st != KVX_OK)
+        return st;
+    pack(src, dst, sizes, n, s->host);
+    cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
+                                    cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        ring_release(dev, s, stream, false);
+        return cuda_fail(e, "cudaMemcpyAsync(chunk table)");
+    }
+    e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, stream);
+    ring_release(dev, s, stream, true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy kernel launch");
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_batch(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                          int dir, int cta_budget, void *stream)
+{
+    if (cta_budget < 0)
+        return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", cta_budget);
+    kvx_launch l{};
+    l.cta_budget = cta_budget;
+    return kvx_copy_batch_ex(src, dst, sizes, n, dir, &l, stream);
+}
+
+kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
+{
+    if (!out)
+        return fail(KVX_ERR_INVALID_ARG, "null output");
+    *out = nullptr;
+    if (max_chunks < 1 || max_chunks > KVX_MAX_CHUNKS)
+        return fail(KVX_ERR_CAPACITY, "max_chunks %zu not in 1..KVX_MAX_CHUNKS", max_chunks);
+    kvx_desc_buf *b = new (std::nothrow) kvx_desc_buf;
+    if (!b)
+        return fail(KVX_ERR_CAPACITY, "out of host memory");
+    cudaError_t e = cudaGetDevice(&b->device);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&b->dev), max_chunks * sizeof(kvx_chunk));
+    if (e == cudaSuccess)
+        e = cudaHostAlloc(reinterpret_cast<void **>(&b->host), max_chunks * sizeof(kvx_chunk),
+                          cudaHostAllocPortable);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&b->upload_done, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&b->last_use, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (b->dev)
+            cudaFree(b->dev);
+        if (b->host)
+            cudaFreeHost(b->host);
+        if (b->upload_done)
+            cudaEventDestroy(b->upload_done);
+        delete b;
+        return cuda_fail(e, "kvx_desc_buf_create");
+    }
+    b->cap = max_chunks;
+    *out = b;
+    return KVX_OK;
+}
+
+kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const uint64_t *dst,
+                                  const uint64_t *sizes, size_t n, int dir, void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!b)
+        return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    uint64_t chunks = 0, payload = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    if (st != KVX_OK)
+        return st;
+    if (chunks > b->cap)
+        return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, buffer holds %zu",
+                    (unsigned long long)chunks, b->cap);
+    Launch l;
+    st = resolve(dir, chunks ? payload / chunks : 0, nullptr, &l);
+    if (st != KVX_OK)
+        return st;
+    bool cap = false;
+    st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
+    if (cap)
+        return fail(KVX_ERR_CAPTURE, "kvx_upload_descriptors writes host staging memory");
+    std::lock_guard<std::mutex> g(b->mu);
+    if (b->upload_recorded) {
+        KVX_CUDA_TRY(cudaEventSynchronize(b->upload_done));
+        b->upload_recorded = false;
+    }
+    pack(src, dst, sizes, n, b->host);
+    if (chunks)
+        KVX_CUDA_TRY(cudaMemcpyAsync(b->dev, b->host, (size_t)chunks * sizeof(kvx_chunk),
+                                     cudaMemcpyHostToDevice, stream));
+    KVX_CUDA_TRY(cudaEventRecord(b->upload_done, stream));
+    b->upload_recorded = true;
+    b->n_chunks = (uint32_t)chunks;
+    b->payload = payload;
+    b->dir = dir;
+    b->selected = {l.variant, l.ctas, l.threads, l.unroll, l.stages, l.store_policy};
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!b)
+        return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    kvx_launch merged = b->selected;
+    if (want) {
+        if (want->variant < 0 || want->variant > KVX_VARIANT_BULK || want->cta_budget < 0)
+            return fail(KVX_ERR_INVALID_ARG, "bad variant %d or cta_budget %d", want->variant,
+                        want->cta_budget);
+        if (want->variant)
+            merged.variant = want->variant;
+        if (want->cta_budget)
+            merged.cta_budget = want->cta_budget;
+        if (want->threads)
+            merged.threads = want->threads;
+        if (want->unroll)
+            merged.unroll = want->unroll;
+        if (want->stages)
+            merged.stages = want->stages;
+        if (want->store_policy)
+            merged.store_policy = want->store_policy;
+    }
+    Launch l;
+    st = resolve(b->dir, 0, &merged, &l);
+    if (st != KVX_OK)
+        return st;
+    if (b->n_chunks == 0)
+        return KVX_OK;
+    bool cap = false;
+    st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
+    cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy kernel launch");
+    if (!cap) {
+        KVX_CUDA_TRY(cudaEventRecord(b->last_use, stream));
+        b->use_recorded = true;
+    }
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_uploaded(kvx_desc_buf *b, int cta_budget, void *stream)
+{
+    if (cta_budget < 0)
+        return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", cta_budget);
+    kvx_launch l{};
+    l.cta_budget = cta_budget;
+    return kvx_copy_uploaded_ex(b, &l, stream);
+}
+
+kvx_status kvx_desc_buf_info(const kvx_desc_buf *b, size_t *n_chunks, uint64_t *payload,
+                             kvx_launch *selected)
+{
+    if (!b)
+        return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    if (n_chunks)
+        *n_chunks = b->n_chunks;
+    if (payload)
+        *payload = b->payload;
+    if (selected)
+        *selected = b->selected;
+    return KVX_OK;
+}
+
+kvx_status kvx_desc_buf_destroy(kvx_desc_buf *b)
+{
+    if (!b)
+        return KVX_OK;
+    if (b->upload_recorded)
+        cudaEventSynchronize(b->upload_done);
+    if (b->use_recorded)
+        cudaEventSynchronize(b->last_use);
+    cudaFree(b->dev);
+    cudaFreeHost(b->host);
+    cudaEventDestroy(b->upload_done);
+    cudaEventDestroy(b->last_use);
+    delete b;
+    return KVX_OK;
+}
+
+kvx_status kvx_stream_check(void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
+    StatusWords &w = g_status_words[dev];
+    unsigned *word = nullptr;
+    {
+        std::lock_guard<std::mutex> g(w.mu);
+        if (!w.words)
+            KVX_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void **>(&w.words),
+                                       kStatusWords * sizeof(unsigned),
+                                       cudaHostAllocMapped | cudaHostAllocPortable));
+        word = w.words + (w.next++ % kStatusWords);
+    }
+    *word = 0;
+    KVX_CUDA_TRY(kvx::launch_status_fetch(word, stream));
+    KVX_CUDA_TRY(cudaStreamSynchronize(stream));
+    const unsigned bits = *reinterpret_cast<volatile unsigned *>(word);
+    if (bits & kvx::kDevErrTimeout)
+        return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
+    if (bits)
+        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x", bits);
+    return KVX_OK;
+}
+
+kvx_status kvx_host_alloc(size_t bytes, void **out)
+{
+    if (!out || !bytes)
+        return fail(KVX_ERR_INVALID_ARG, "null output or zero bytes");
+    *out = nullptr;
+    void *p = nullptr;
+    KVX_CUDA_TRY(cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    void *dp = nullptr;
+    cudaError_t e = cudaHostGetDevicePointer(&dp, p, 0);
+    if (e != cudaSuccess || dp != p) {
+        cudaFreeHost(p);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaHostGetDevicePointer");
+        return fail(KVX_ERR_NOT_MAPPED, "device address of pinned memory differs from its host address");
+    }
+    *out = p;
+    return KVX_OK;
+}
+
+kvx_status kvx_host_free(void *p)
+{
+    if (!p)
+        return KVX_OK;
+    KVX_CUDA_TRY(cudaFreeHost(p));
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_batch_memcpy(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes,
+                                 size_t n, int dir, void *stream_, size_t *n_ranges)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    st = validate(src, dst, sizes, n, dir, validate_level(), nullptr, nullptr);
+    if (st != KVX_OK)
+        return st;
+    const cudaMemcpyKind kind = dir == KVX_H2D   ? cudaMemcpyHostToDevice
+                                : dir == KVX_D2H ? cudaMemcpyDeviceToHost
+                                                 : cudaMemcpyDeviceToDevice;
+    size_t ranges = 0;
+    size_t i = 0;
+    while (i < n) {
+        if (!sizes[i]) {
+            ++i;
+            continue;
+        }
+        uint64_t s = src[i], d = dst[i], z = sizes[i];
+        size_t k = i + 1;
+        while (k < n && sizes[k] && src[k] == s + z && dst[k] == d + z) {
+            z += sizes[k];
+            ++k;
+        }
+        KVX_CUDA_TRY(cudaMemcpyAsync(reinterpret_cast<void *>(d), reinterpret_cast<const void *>(s),
+                                     (size_t)z, kind, stream));
+        ++ranges;
+        i = k;
+    }
+    if (n_ranges)
+        *n_ranges = ranges;
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int dir, void *stream)
+{
+    if (dir < KVX_H2D || dir > KVX_D2D)
+        return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
+    if (!bytes)
+        return KVX_OK;
+    if (!src || !dst)
+        return fail(KVX_ERR_INVALID_ARG, "null address");
+    const cudaMemcpyKind kind = dir == KVX_H2D   ? cudaMemcpyHostToDevice
+                                : dir == KVX_D2H ? cudaMemcpyDeviceToHost
+                                                 : cudaMemcpyDeviceToDevice;
+    KVX_CUDA_TRY(cudaMemcpyAsync(reinterpret_cast<void *>(dst), reinterpret_cast<const void *>(src),
+                                 (size_t)bytes, kind, static_cast<cudaStream_t>(stream)));
+    return KVX_OK;
+}
+
+kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
+{
+    if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull)
+        return fail(KVX_ERR_INVALID_ARG, "timeout_ns %llu not in [1 ms, 10 s]",
+                    (unsigned long long)timeout_ns);
+    KVX_CUDA_TRY(kvx::launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream)));
+    return KVX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Internal interface between the host engine (kvx_engine.cu) and the device
+// kernels (kvx_kernels.cu). Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvx.h"
+
+static_assert(sizeof(kvx_chunk) == 32, "chunk records are 32 bytes");
+
+namespace kvx {
+
+// Bits of the device status word (one per device, shared by all streams).
+enum : unsigned {
+    kDevErrTimeout = 1u,    // a bounded mbarrier wait gave up
+    kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES
+};
+
+// Bounded-wait limit of the bulk kernel's mbarrier waits (ns of %globaltimer).
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+// A resolved launch: every field set.
+struct Launch {
+    int variant;       // KVX_VARIANT_LDG or KVX_VARIANT_BULK
+    int ctas;          // grid size (already clamped to the work)
+    int threads;       // LDG threads per CTA
+    int unroll;        // LDG 16-byte loads in flight per lane
+    int stages;        // BULK ring stages
+    int store_policy;  // LDG store cache policy
+};
+
+// Grid needed to give every CTA some work, for a chunk count and variant.
+int work_ctas(const Launch &l, uint32_t n_chunks);
+
+// Enqueue the copy kernel over a device-resident chunk table.
+cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
+                        cudaStream_t stream);
+
+// Enqueue a 1-thread kernel that moves the status word into *host_word
+// (mapped pinned) and clears it.
+cudaError_t launch_status_fetch(unsigned *host_word, cudaStream_t stream);
+
+// Enqueue the bounded-wait self-test kernel.
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+
+// Shared memory the bulk kernel needs for `stages` stages.
+size_t bulk_smem_bytes(int stages);
+
+}  // namespace kvx

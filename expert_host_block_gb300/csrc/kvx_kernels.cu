@@ -1,0 +1,515 @@
+// Copy kernels of kvx for sm_103a.
+//
+// Both variants walk the same device-resident table of 32-byte chunk records
+// ({src, dst, len <= 16 KiB, desc}) as a persistent grid: work unit c goes to
+// worker (c mod workers), where a worker is a warp (LDG) or a CTA (BULK).
+// Chunks are at most 16 KiB, so handing them out round-robin spreads the
+// batch's bytes evenly over the workers, whatever mix of descriptor sizes it
+// holds (FreeToken issue #751, §Problem in upstream today and §What we
+// changed: split the call's bytes, not its banks, over the CTAs).
+//
+// LDG variant: every lane moves 16-byte words, `U` loads in flight per lane
+// before the matching stores (the pages' LDG kernel keeps one 16-byte load in
+// flight per thread; FreeToken issue #751, §Problem in upstream today). A warp
+// reads the records of its next 32 chunks with one load per lane and passes
+// them around with shuffles, so no lane waits on a record load per chunk.
+//
+// BULK variant: one warp per CTA; lane 0 streams chunks through an S-stage
+// ring of 16 KiB shared::cta buffers with cp.async.bulk loads completed on an
+// mbarrier, then cp.async.bulk stores (FreeToken issue #751, §What we changed:
+// a 3-stage ring, one issuing thread per CTA, the .shared::cta destination
+// form). Every mbarrier wait is bounded by %globaltimer.
+//
+// Unaligned pieces: addresses and sizes are multiples of 8. When src and dst
+// have the same phase mod 16, a chunk is an 8-byte head, a 16-byte-word body
+// and an 8-byte tail; otherwise the whole chunk moves as 8-byte words.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvx_internal.h"
+
+namespace kvx {
+
+__device__ unsigned g_status;
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- global memory access (inline PTX) ----------------------------------
+
+__device__ __forceinline__ uint4 ld16(const unsigned char *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld8(const unsigned char *p)
+{
+    uint2 v;
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+template <int P>
+__device__ __forceinline__ void st16(unsigned char *p, uint4 v)
+{
+    if constexpr (P == 1)
+        asm volatile("st.global.wt.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+    else if constexpr (P == 2)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+}
+
+template <int P>
+__device__ __forceinline__ void st8(unsigned char *p, uint2 v)
+{
+    if constexpr (P == 1)
+        asm volatile("st.global.wt.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    else if constexpr (P == 2)
+        asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    else
+        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// ---- one chunk, moved by one warp ---------------------------------------
+
+template <int U, int P>
+__device__ __forceinline__ void copy_chunk_warp(uint64_t s, uint64_t d, uint32_t len,
+                                                uint32_t lane)
+{
+    if (len == 0)
+        return;
+    if (((s ^ d) & 15u) == 0) {
+        if (s & 15u) {  // 8-byte head up to the 16-byte boundary
+            if (lane == 0)
+                st8<P>(reinterpret_cast<unsigned char *>(d),
+                       ld8(reinterpret_cast<const unsigned char *>(s)));
+            s += 8;
+            d += 8;
+            len -= 8;
+        }
+        const uint32_t n16 = len >> 4;
+        if ((len & 15u) && lane == 1) {  // 8-byte tail
+            const uint64_t o = (uint64_t)n16 << 4;
+            st8<P>(reinterpret_cast<unsigned char *>(d + o),
+                   ld8(reinterpret_cast<const unsigned char *>(s + o)));
+        }
+        const unsigned char *S = reinterpret_cast<const unsigned char *>(s);
+        unsigned char *D = reinterpret_cast<unsigned char *>(d);
+        for (uint32_t i0 = 0; i0 < n16; i0 += 32u * U) {
+            uint4 r[U];
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const uint32_t idx = i0 + 32u * j + lane;
+                if (idx < n16)
+                    r[j] = ld16(S + ((uint64_t)idx << 4));
+            }
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+                const uint32_t idx = i0 + 32u * j + lane;
+                if (idx < n16)
+                    st16<P>(D + ((uint64_t)idx << 4), r[j]);
+            }
+        }
+    } else {  // source and destination phases differ: 8-byte words throughout
+        const uint32_t n8 = len >> 3;
+        const unsigned char *S = reinterpret_cast<const unsigned char *>(s);
+        unsigned char *D = reinterpret_cast<unsigned char *>(d);
+        for (uint32_t i0 = 0; i0 < n8; i0 += 64u * U) {
+            uint2 r[2 * U];
+#pragma unroll
+            for (int j = 0; j < 2 * U; ++j) {
+                const uint32_t idx = i0 + 32u * j + lane;
+                if (idx < n8)
+                    r[j] = ld8(S + ((uint64_t)idx << 3));
+            }
+#pragma unroll
+            for (int j = 0; j < 2 * U; ++j) {
+                const uint32_t idx = i0 + 32u * j + lane;
+                if (idx < n8)
+                    st8<P>(D + ((uint64_t)idx << 3), r[j]);
+            }
+        }
+    }
+}
+
+// A chunk record held in one lane's registers.
+struct Rec {
+    uint64_t s, d;
+    uint32_t l;
+};
+
+__device__ __forceinline__ Rec load_rec(const kvx_chunk *__restrict__ tab, uint64_t c)
+{
+    const uint4 *p = reinterpret_cast<const uint4 *>(tab + c);
+    const uint4 a = __ldg(p);
+    const uint4 b = __ldg(p + 1);
+    Rec r;
+    r.s = (uint64_t)a.x | ((uint64_t)a.y << 32);
+    r.d = (uint64_t)a.z | ((uint64_t)a.w << 32);
+    r.l = b.x;
+    if (r.l > KVX_CHUNK_BYTES) {  // never produced by the host planner
+        atomicOr(&g_status, kDevErrBadRecord);
+        r.l = 0;
+    }
+    return r;
+}
+
+__device__ __forceinline__ Rec shfl_rec(const Rec &r, int src_lane)
+{
+    Rec o;
+    o.s = __shfl_sync(kFull, r.s, src_lane);
+    o.d = __shfl_sync(kFull, r.d, src_lane);
+    o.l = __shfl_sync(kFull, r.l, src_lane);
+    return o;
+}
+
+// ---- LDG variant -----------------------------------------------------------
+
+template <int U, int P>
+__global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
+                                                            uint32_t n_chunks)
+{
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t wpb = blockDim.x >> 5;
+    const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
+    // Chunks of this warp: gwarp + k * nwarps. Each pass takes 32 of them; lane l
+    // loads the record of the l-th.
+    for (uint64_t base = gwarp; base < n_chunks; base += 32u * nwarps) {
+        const uint64_t mine = base + (uint64_t)lane * nwarps;
+        Rec r = {0, 0, 0};
+        if (mine < n_chunks)
+            r = load_rec(tab, mine);
+        const int cnt = __popc(__ballot_sync(kFull, mine < n_chunks));
+        for (int k = 0; k < cnt; ++k) {
+            const Rec c = shfl_rec(r, k);
+            copy_chunk_warp<U, P>(c.s, c.d, c.l, lane);
+        }
+    }
+}
+
+// ---- BULK variant ----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the mbarrier to complete, giving up after
+// limit_ns of %globaltimer (or 2^28 polls, whichever comes first).
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 31u) == 31u && globaltimer() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, uint64_t src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_smem),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(uint64_t dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ bool bulk_ok(const Rec &r)
+{
+    return r.l != 0 && ((r.s | r.d | (uint64_t)r.l) & 15u) == 0;
+}
+
+template <int S>
+__global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__restrict__ tab,
+                                                           uint32_t n_chunks, uint64_t wait_ns)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t bars[S];
+    const uint32_t lane = threadIdx.x;
+    const uint32_t ring0 = smem_u32(ring);
+    const uint32_t bar0 = smem_u32(bars);
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s)
+            mbar_init(bar0 + 8u * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    // Chunks of this CTA: blockIdx.x + k * gridDim.x, k in [0, my_n).
+    const uint64_t my_n =
+        n_chunks > blockIdx.x ? (n_chunks - 1ull - blockIdx.x) / gridDim.x + 1ull : 0ull;
+    auto chunk_of = [&](uint64_t k) { return (uint64_t)blockIdx.x + k * gridDim.x; };
+    auto load_batch = [&](uint64_t k0) {
+        Rec r = {0, 0, 0};
+        if (k0 + lane < my_n)
+            r = load_rec(tab, chunk_of(k0 + lane));
+        return r;
+    };
+    // Records of chunks [a0, a0+32) in batch A and [a0+32, a0+64) in batch B.
+    uint64_t a0 = 0;
+    Rec A = load_batch(0);
+    Rec B = load_batch(32);
+    auto fetch = [&](uint64_t k) {
+        const Rec x = shfl_rec(A, (int)((k - a0) & 31u));
+        const Rec y = shfl_rec(B, (int)((k - a0) & 31u));
+        return (k - a0 < 32u) ? x : y;
+    };
+
+    uint32_t phase = 0;    // bit s: parity of the next completion of stage s
+    uint32_t pending = 0;  // bit s: a load is in flight on stage s
+    bool timed_out = false;
+
+    for (int j = 0; j < S - 1; ++j) {  // prologue: fill S-1 stages
+        if ((uint64_t)j < my_n) {
+            const Rec r = fetch(j);
+            if (bulk_ok(r)) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar0 + 8u * j, r.l);
+                    bulk_load(ring0 + (uint32_t)j * KVX_CHUNK_BYTES, r.s, r.l, bar0 + 8u * j);
+                }
+                pending |= 1u << j;
+            }
+        }
+    }
+
+    for (uint64_t k = 0; k < my_n; ++k) {
+        if (k == a0 + 32) {  // slide the record window
+            A = B;
+            a0 += 32;
+            B = load_batch(a0 + 32);
+        }
+        const Rec r = fetch(k);
+        const int st = (int)(k % S);
+        bool stored = false;
+        if (bulk_ok(r)) {
+            // Lane 0 waits; the outcome is broadcast so the warp stays converged.
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait_bounded(bar0 + 8u * st, (phase >> st) & 1u, wait_ns);
+            if (!__shfl_sync(kFull, (int)ok, 0)) {
+                timed_out = true;
+                break;
+            }
+            phase ^= 1u << st;
+            pending &= ~(1u << st);
+            if (lane == 0) {
+                bulk_store(r.d, ring0 + (uint32_t)st * KVX_CHUNK_BYTES, r.l);
+                bulk_commit();
+            }
+            stored = true;
+        } else {
+            copy_chunk_warp<4, 0>(r.s, r.d, r.l, lane);
+        }
+        const uint64_t j = k + S - 1;
+        if (j < my_n) {
+            const Rec n = fetch(j);
+            if (bulk_ok(n)) {
+                const int sj = (int)(j % S);  // == (k - 1) mod S: the stage chunk k-1 used
+                if (lane == 0) {
+                    if (stored)
+                        bulk_wait_read<1>();
+                    else
+                        bulk_wait_read<0>();
+                    mbar_arrive_expect_tx(bar0 + 8u * sj, n.l);
+                    bulk_load(ring0 + (uint32_t)sj * KVX_CHUNK_BYTES, n.s, n.l, bar0 + 8u * sj);
+                }
+                pending |= 1u << sj;
+            }
+        }
+    }
+
+    if (timed_out) {
+        if (lane == 0)
+            atomicOr(&g_status, kDevErrTimeout);
+        // Let the loads still in flight land before the shared memory goes away.
+        if (lane == 0)
+            for (int s = 0; s < S; ++s)
+                if (pending & (1u << s))
+                    mbar_wait_bounded(bar0 + 8u * s, (phase >> s) & 1u, wait_ns);
+    }
+    if (lane == 0)
+        bulk_wait_all();
+    __syncwarp();
+}
+
+// ---- status word and the bounded-wait self-test ---------------------------
+
+__global__ void kvx_status_fetch_kernel(unsigned *host_word)
+{
+    *host_word = atomicExch(&g_status, 0u);
+    __threadfence_system();
+}
+
+__global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    // Nothing arrives on the barrier, so phase 0 never completes.
+    if (threadIdx.x == 0 && !mbar_wait_bounded(b, 0, timeout_ns))
+        atomicOr(&g_status, kDevErrTimeout);
+    __syncwarp();
+}
+
+template <int U, int P>
+cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, cudaStream_t s)
+{
+    kvx_copy_ldg_kernel<U, P><<<ctas, threads, 0, s>>>(t, n);
+    return cudaGetLastError();
+}
+
+template <int U>
+cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint32_t n,
+                         cudaStream_t s)
+{
+    switch (p) {
+    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, s);
+    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, s);
+    default: return launch_ldg<U, 0>(ctas, threads, t, n, s);
+    }
+}
+
+template <int S>
+cudaError_t launch_bulk(int ctas, const kvx_chunk *t, uint32_t n, cudaStream_t s)
+{
+    const size_t smem = bulk_smem_bytes(S);
+    cudaError_t e = cudaFuncSetAttribute(kvx_copy_bulk_kernel<S>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kvx_copy_bulk_kernel<S><<<ctas, 32, smem, s>>>(t, n, kBulkWaitNs);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bulk_smem_bytes(int stages) { return (size_t)stages * KVX_CHUNK_BYTES; }
+
+int work_ctas(const Launch &l, uint32_t n_chunks)
+{
+    uint64_t need;
+    if (l.variant == KVX_VARIANT_BULK)
+        need = n_chunks;
+    else
+        need = (n_chunks + (uint64_t)(l.threads / 32) - 1) / (uint64_t)(l.threads / 32);
+    if (need < 1)
+        need = 1;
+    return (int)((uint64_t)l.ctas < need ? (uint64_t)l.ctas : need);
+}
+
+cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
+                        cudaStream_t stream)
+{
+    if (n_chunks == 0)
+        return cudaSuccess;
+    const int ctas = work_ctas(l, n_chunks);
+    if (l.variant == KVX_VARIANT_BULK) {
+        switch (l.stages) {
+        case 2: return launch_bulk<2>(ctas, table, n_chunks, stream);
+        case 4: return launch_bulk<4>(ctas, table, n_chunks, stream);
+        default: return launch_bulk<3>(ctas, table, n_chunks, stream);
+        }
+    }
+    switch (l.unroll) {
+    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
+    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
+    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
+    }
+}
+
+cudaError_t launch_status_fetch(unsigned *host_word, cudaStream_t stream)
+{
+    kvx_status_fetch_kernel<<<1, 1, 0, stream>>>(host_word);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream)
+{
+    kvx_wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace kvx

@@ -1,0 +1,368 @@
+"""Python binding of libkvx.so: the C ABI of ``include/kvx.h`` under the same names.
+
+Argument marshalling only: every step of a copy (validation, chunking,
+packing, upload, the copy kernel) runs inside libkvx.so. Descriptor arrays
+are numpy ``uint64`` arrays (or anything ``np.asarray`` turns into one);
+streams are ``torch.cuda.Stream`` objects, raw ``cudaStream_t`` integers, or
+``None`` for the legacy default stream. A non-OK status raises ``KvxError``
+carrying the status and the library's message.
+
+The library must have been built (``__graft_entry__.build()`` or
+``python -m expert_host_block_gb300.build``); importing this module without
+it raises at once. There is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+KVX_H2D, KVX_D2H, KVX_D2D = 0, 1, 2
+DIRS = {"h2d": KVX_H2D, "d2h": KVX_D2H, "d2d": KVX_D2D}
+KVX_VARIANT_AUTO, KVX_VARIANT_LDG, KVX_VARIANT_BULK = 0, 1, 2
+VARIANTS = {"auto": KVX_VARIANT_AUTO, "ldg": KVX_VARIANT_LDG, "bulk": KVX_VARIANT_BULK}
+
+KVX_OK = 0
+KVX_ERR_INVALID_ARG = 1
+KVX_ERR_ALIGN = 2
+KVX_ERR_OVERLAP = 3
+KVX_ERR_CAPACITY = 4
+KVX_ERR_NOT_MAPPED = 5
+KVX_ERR_CUDA = 6
+KVX_ERR_TIMEOUT = 7
+KVX_ERR_DEVICE_FAULT = 8
+KVX_ERR_CAPTURE = 9
+
+KVX_CHUNK_BYTES = 16384
+KVX_MAX_CHUNKS = 1 << 22
+
+CHUNK_DTYPE = np.dtype([("src", "<u8"), ("dst", "<u8"), ("len", "<u4"), ("desc", "<u4"),
+                        ("reserved", "<u8")])
+
+# Every symbol include/kvx.h declares.
+EXPORTS = (
+    "kvx_copy_batch", "kvx_copy_batch_ex", "kvx_desc_buf_create", "kvx_upload_descriptors",
+    "kvx_copy_uploaded", "kvx_copy_uploaded_ex", "kvx_desc_buf_info", "kvx_desc_buf_destroy",
+    "kvx_validate", "kvx_plan_chunks", "kvx_default_launch", "kvx_set_validate_level",
+    "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version",
+    "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
+    "kvx_copy_contiguous", "kvx_selftest_wait_timeout",
+)
+
+
+class kvx_launch(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("cta_budget", ctypes.c_int), ("threads", ctypes.c_int),
+                ("unroll", ctypes.c_int), ("stages", ctypes.c_int), ("store_policy", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class KvxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{self.name}: {message}")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_u64 = ctypes.c_uint64
+_int = ctypes.c_int
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` (no fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "kvx_copy_batch": ([_vp, _vp, _vp, _sz, _int, _int, _vp], _int),
+        "kvx_copy_batch_ex": ([_vp, _vp, _vp, _sz, _int, ctypes.POINTER(kvx_launch), _vp], _int),
+        "kvx_desc_buf_create": ([_sz, ctypes.POINTER(_vp)], _int),
+        "kvx_upload_descriptors": ([_vp, _vp, _vp, _vp, _sz, _int, _vp], _int),
+        "kvx_copy_uploaded": ([_vp, _int, _vp], _int),
+        "kvx_copy_uploaded_ex": ([_vp, ctypes.POINTER(kvx_launch), _vp], _int),
+        "kvx_desc_buf_info": ([_vp, ctypes.POINTER(_sz), ctypes.POINTER(_u64), ctypes.POINTER(kvx_launch)], _int),
+        "kvx_desc_buf_destroy": ([_vp], _int),
+        "kvx_validate": ([_vp, _vp, _vp, _sz, _int, _int], _int),
+        "kvx_plan_chunks": ([_vp, _vp, _vp, _sz, _vp, _sz, ctypes.POINTER(_sz)], _int),
+        "kvx_default_launch": ([_int, _u64, ctypes.POINTER(kvx_launch)], _int),
+        "kvx_set_validate_level": ([_int], _int),
+        "kvx_get_validate_level": ([], _int),
+        "kvx_status_string": ([_int], ctypes.c_char_p),
+        "kvx_last_error": ([], ctypes.c_char_p),
+        "kvx_version": ([], _int),
+        "kvx_stream_check": ([_vp], _int),
+        "kvx_host_alloc": ([_sz, ctypes.POINTER(_vp)], _int),
+        "kvx_host_free": ([_vp], _int),
+        "kvx_copy_batch_memcpy": ([_vp, _vp, _vp, _sz, _int, _vp, ctypes.POINTER(_sz)], _int),
+        "kvx_copy_contiguous": ([_u64, _u64, _u64, _int, _vp], _int),
+        "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def lib():
+    """The loaded ctypes library (raises if it was not built)."""
+    return _load()
+
+
+def status_string(status: int) -> str:
+    return _load().kvx_status_string(status).decode()
+
+
+def last_error() -> str:
+    return _load().kvx_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != KVX_OK:
+        raise KvxError(status, last_error())
+
+
+def _u64arr(a) -> np.ndarray:
+    if isinstance(a, np.ndarray) and a.dtype == np.uint64 and a.flags.c_contiguous:
+        return a
+    if hasattr(a, "numpy") and not isinstance(a, np.ndarray):  # torch CPU tensor
+        a = a.numpy()
+    return np.ascontiguousarray(np.asarray(a).astype(np.uint64, copy=False).reshape(-1))
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    raise TypeError(f"not a stream: {s!r}")
+
+
+def _triple(src_addrs, dst_addrs, sizes, n):
+    s, d, z = _u64arr(src_addrs), _u64arr(dst_addrs), _u64arr(sizes)
+    if n is None:
+        n = z.size
+    if not (s.size >= n and d.size >= n and z.size >= n):
+        raise ValueError(f"descriptor arrays shorter than n = {n}")
+    return s, d, z, int(n)
+
+
+def _launch(launch) -> kvx_launch | None:
+    if launch is None:
+        return None
+    if isinstance(launch, kvx_launch):
+        return launch
+    v = dict(launch)
+    if isinstance(v.get("variant"), str):
+        v["variant"] = VARIANTS[v["variant"]]
+    return kvx_launch(**v)
+
+
+def _dir(d) -> int:
+    return DIRS[d] if isinstance(d, str) else int(d)
+
+
+# ---- the batch copy --------------------------------------------------------
+
+def kvx_copy_batch(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, cta_budget=0, stream=None) -> None:
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    _check(_load().kvx_copy_batch(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                  int(cta_budget), _stream(stream)))
+
+
+def kvx_copy_batch_ex(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, launch=None, stream=None) -> None:
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    lp = _launch(launch)
+    _check(_load().kvx_copy_batch_ex(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                     ctypes.byref(lp) if lp is not None else None, _stream(stream)))
+
+
+# ---- descriptor buffers ----------------------------------------------------
+
+def kvx_desc_buf_create(max_chunks: int) -> int:
+    h = _vp()
+    _check(_load().kvx_desc_buf_create(int(max_chunks), ctypes.byref(h)))
+    return h.value
+
+
+def kvx_upload_descriptors(buf: int, src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, stream=None) -> None:
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    _check(_load().kvx_upload_descriptors(buf, s.ctypes.data, d.ctypes.data, z.ctypes.data, n,
+                                          _dir(dir), _stream(stream)))
+
+
+def kvx_copy_uploaded(buf: int, cta_budget=0, stream=None) -> None:
+    _check(_load().kvx_copy_uploaded(buf, int(cta_budget), _stream(stream)))
+
+
+def kvx_copy_uploaded_ex(buf: int, launch=None, stream=None) -> None:
+    lp = _launch(launch)
+    _check(_load().kvx_copy_uploaded_ex(buf, ctypes.byref(lp) if lp is not None else None,
+                                        _stream(stream)))
+
+
+def kvx_desc_buf_info(buf: int):
+    """(n_chunks, payload_bytes, selected launch as a dict)."""
+    n, p, l = _sz(), _u64(), kvx_launch()
+    _check(_load().kvx_desc_buf_info(buf, ctypes.byref(n), ctypes.byref(p), ctypes.byref(l)))
+    return n.value, p.value, l.as_dict()
+
+
+def kvx_desc_buf_destroy(buf: int) -> None:
+    _check(_load().kvx_desc_buf_destroy(buf))
+
+
+class DescBuf:
+    """A kvx_desc_buf owned by a Python object."""
+
+    def __init__(self, max_chunks: int):
+        self.handle = kvx_desc_buf_create(max_chunks)
+        self.max_chunks = int(max_chunks)
+
+    def upload(self, src_addrs, dst_addrs, sizes, dir, stream=None):
+        kvx_upload_descriptors(self.handle, src_addrs, dst_addrs, sizes, None, dir, stream)
+
+    def copy(self, cta_budget=0, stream=None, launch=None):
+        if launch is None:
+            kvx_copy_uploaded(self.handle, cta_budget, stream)
+        else:
+            kvx_copy_uploaded_ex(self.handle, launch, stream)
+
+    def info(self):
+        return kvx_desc_buf_info(self.handle)
+
+    def close(self):
+        if self.handle:
+            kvx_desc_buf_destroy(self.handle)
+            self.handle = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- host-only helpers -----------------------------------------------------
+
+def kvx_validate(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, level=0) -> int:
+    """The status kvx_copy_batch would return before enqueuing (does not raise)."""
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    return int(_load().kvx_validate(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir), int(level)))
+
+
+def kvx_plan_chunks(src_addrs, dst_addrs, sizes, n=None) -> np.ndarray:
+    """The chunk table (structured array of CHUNK_DTYPE) kvx would upload."""
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    cnt = _sz()
+    L = _load()
+    _check(L.kvx_plan_chunks(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, None, 0, ctypes.byref(cnt)))
+    out = np.zeros(cnt.value, dtype=CHUNK_DTYPE)
+    _check(L.kvx_plan_chunks(s.ctypes.data, d.ctypes.data, z.ctypes.data, n,
+                             out.ctypes.data if out.size else None, out.size, ctypes.byref(cnt)))
+    return out
+
+
+def kvx_default_launch(dir, mean_chunk_bytes: int) -> dict:
+    l = kvx_launch()
+    _check(_load().kvx_default_launch(_dir(dir), int(mean_chunk_bytes), ctypes.byref(l)))
+    return l.as_dict()
+
+
+def kvx_set_validate_level(level: int) -> None:
+    _check(_load().kvx_set_validate_level(int(level)))
+
+
+def kvx_get_validate_level() -> int:
+    return int(_load().kvx_get_validate_level())
+
+
+def kvx_version() -> int:
+    return int(_load().kvx_version())
+
+
+# ---- device status, memory -------------------------------------------------
+
+def kvx_stream_check(stream=None) -> None:
+    _check(_load().kvx_stream_check(_stream(stream)))
+
+
+def kvx_host_alloc(nbytes: int) -> int:
+    p = _vp()
+    _check(_load().kvx_host_alloc(int(nbytes), ctypes.byref(p)))
+    return p.value
+
+
+def kvx_host_free(addr: int) -> None:
+    _check(_load().kvx_host_free(addr))
+
+
+class HostBuffer:
+    """Mapped pinned host memory from kvx_host_alloc, viewable as a numpy array."""
+
+    def __init__(self, nbytes: int):
+        self.nbytes = int(nbytes)
+        self.addr = kvx_host_alloc(self.nbytes)
+        self._view = np.ctypeslib.as_array((ctypes.c_uint8 * self.nbytes).from_address(self.addr))
+
+    def numpy(self) -> np.ndarray:
+        return self._view
+
+    def close(self):
+        if self.addr:
+            self._view = None
+            kvx_host_free(self.addr)
+            self.addr = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- baselines -------------------------------------------------------------
+
+def kvx_copy_batch_memcpy(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, stream=None) -> int:
+    """Per-range directional cudaMemcpyAsync; returns the number of memcpy calls."""
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    r = _sz()
+    _check(_load().kvx_copy_batch_memcpy(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                         _stream(stream), ctypes.byref(r)))
+    return r.value
+
+
+def kvx_copy_contiguous(dst: int, src: int, nbytes: int, dir, stream=None) -> None:
+    _check(_load().kvx_copy_contiguous(int(dst), int(src), int(nbytes), _dir(dir), _stream(stream)))
+
+
+def kvx_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(_load().kvx_selftest_wait_timeout(int(timeout_ns), _stream(stream)))

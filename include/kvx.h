@@ -1,0 +1,241 @@
+/*
+ * kvx: batched, descriptor-driven scatter/gather copies between mapped pinned
+ * host memory and HBM, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation. A batch is n descriptors (src_i, dst_i, size_i). The result
+ * of a batch is the result of one memcpy(dst_i, src_i, size_i) per
+ * descriptor; no other byte changes. The pages replace one directional CUDA
+ * memcpy per fragment with one descriptor upload and one copy-kernel launch
+ * (PegaFlow issue #408, "Kernel transfer backend causes decode TPOT tail
+ * spikes under concurrent KV transfers", §Summary), and the copy kernel moves
+ * the same bytes as the path it replaces (FreeToken issue #751, "[Perf]
+ * Offloaded decode: gather missed experts with a few TMA bulk-copy CTAs",
+ * §What we changed; vLLM PR #42212 report, §实现拆解 items 1 and 4).
+ *
+ * How kvx runs a batch. The host validates the descriptors, cuts each one
+ * into chunks of at most KVX_CHUNK_BYTES at 8-byte granularity, packs the
+ * 32-byte chunk records into a pinned staging buffer, uploads the table with
+ * one cudaMemcpyAsync and launches one persistent copy kernel on `stream`
+ * with at most `cta_budget` CTAs. Every call is enqueue-only: it returns once
+ * the work is queued (PegaFlow issue #408, follow-up §2: the transfer
+ * backend contract is enqueue-only and never synchronises).
+ *
+ * Common rules for every entry point below:
+ *   - Addresses are plain 64-bit virtual addresses in the unified address
+ *     space. Host memory must be mapped pinned memory (kvx_host_alloc, or
+ *     cudaHostAlloc with cudaHostAllocMapped on a unified-addressing system)
+ *     so that the device can use the same address. kvx does not translate.
+ *   - src_i, dst_i and size_i must be multiples of 8 (the 8-byte word
+ *     granularity of the vLLM kernel, which the report selects only for
+ *     8-byte-aligned pages: vLLM PR #42212 report, §实现拆解 item 2). kvx
+ *     rejects other values with KVX_ERR_ALIGN instead of truncating them.
+ *     16-byte alignment is not required; it only makes the fast paths apply.
+ *   - Destination ranges of one batch must not overlap one another or any
+ *     source range of the batch. Source ranges may overlap. Under that rule
+ *     the result does not depend on descriptor order, and kvx gives no order
+ *     among descriptors. kvx checks it only at validation level >= 1
+ *     (kvx_set_validate_level); at level 0 an overlapping batch is undefined.
+ *   - A size of 0 is a no-op (its addresses are not checked); n == 0 is a
+ *     no-op that returns KVX_OK.
+ *   - The caller owns all payload memory and the three descriptor arrays.
+ *     The arrays are read during the call only and may be reused when it
+ *     returns. The payload must stay valid until the stream reaches the copy.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream) of the
+ *     device that is current in the calling thread.
+ *   - Errors: a non-KVX_OK status means nothing was enqueued, except
+ *     KVX_ERR_CUDA from a launch, which may follow a completed table upload.
+ *     kvx_last_error() gives a one-line message for the calling thread.
+ *     Device-side errors (a bounded wait that gave up) are reported by
+ *     kvx_stream_check. No entry point aborts the process or traps the GPU.
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVX_VERSION_MAJOR 0
+#define KVX_VERSION_MINOR 1
+
+/* Largest chunk a descriptor is cut into: 16 KiB, the chunk of the FreeToken
+ * gather (FreeToken issue #751, §What we changed: "chunks of up to 16 KiB,
+ * each inside one bank row"). */
+#define KVX_CHUNK_BYTES 16384u
+/* Most chunks one batch may expand to (a 128 MiB chunk table). */
+#define KVX_MAX_CHUNKS (1u << 22)
+
+typedef enum kvx_dir {
+    KVX_H2D = 0, /* mapped pinned host -> device memory */
+    KVX_D2H = 1, /* device memory -> mapped pinned host */
+    KVX_D2D = 2  /* device memory -> device memory */
+} kvx_dir;
+
+typedef enum kvx_variant {
+    KVX_VARIANT_AUTO = 0, /* pick from the calibrated table by direction and size */
+    KVX_VARIANT_LDG = 1,  /* 16-byte loads/stores by every lane, several in flight */
+    KVX_VARIANT_BULK = 2  /* cp.async.bulk through a shared::cta ring, one issuing lane */
+} kvx_variant;
+
+typedef enum kvx_status {
+    KVX_OK = 0,
+    KVX_ERR_INVALID_ARG = 1,  /* null array, bad dir/variant/budget, null address, address overflow */
+    KVX_ERR_ALIGN = 2,        /* an address or size is not a multiple of 8 */
+    KVX_ERR_OVERLAP = 3,      /* (validation level >= 1) destination ranges overlap */
+    KVX_ERR_CAPACITY = 4,     /* more than KVX_MAX_CHUNKS chunks, or more than a buffer holds */
+    KVX_ERR_NOT_MAPPED = 5,   /* (validation level 2) an address is not of the kind dir names */
+    KVX_ERR_CUDA = 6,         /* a CUDA runtime call failed; see kvx_last_error() */
+    KVX_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (reported by kvx_stream_check) */
+    KVX_ERR_DEVICE_FAULT = 8, /* the device reported an inconsistent chunk record */
+    KVX_ERR_CAPTURE = 9       /* the call is not allowed while `stream` is being captured */
+} kvx_status;
+
+/* One chunk record of the uploaded table: 32 bytes. `len` <= KVX_CHUNK_BYTES,
+ * `desc` is the index of the descriptor the chunk belongs to. */
+typedef struct kvx_chunk {
+    uint64_t src;
+    uint64_t dst;
+    uint32_t len;
+    uint32_t desc;
+    uint64_t reserved;
+} kvx_chunk;
+
+/* Launch configuration. Zero in a field means "take it from the calibrated
+ * table" (direction and mean chunk size select the row). */
+typedef struct kvx_launch {
+    int variant;         /* kvx_variant */
+    int cta_budget;      /* maximum CTAs; the grid is min(cta_budget, work) */
+    int threads;         /* LDG: threads per CTA, one of 128, 256, 512 */
+    int unroll;          /* LDG: 16-byte loads in flight per lane, one of 2, 4, 8 */
+    int stages;          /* BULK: ring stages of KVX_CHUNK_BYTES each, 2..4 */
+    int store_policy;    /* LDG: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
+} kvx_launch;
+
+/* Opaque, library-owned reusable descriptor buffer (device chunk table plus
+ * its pinned staging buffer). */
+typedef struct kvx_desc_buf kvx_desc_buf;
+
+/* ---- the batch copy ----------------------------------------------------- */
+
+/* Copy a batch: validate, chunk, pack, upload the chunk table and launch the
+ * copy kernel on `stream`. `dir` is a kvx_dir; it selects the table row and
+ * what validation level 2 checks (data moves through unified addresses in
+ * every direction). `cta_budget`: 0 = calibrated default, > 0 = at most that
+ * many CTAs, < 0 = KVX_ERR_INVALID_ARG. Not allowed during stream capture
+ * (KVX_ERR_CAPTURE): it writes a pinned staging slot on the host. The staging
+ * ring has 8 slots per device; a call waits on the host only when the slot it
+ * takes is still in use by a call eight calls back. */
+kvx_status kvx_copy_batch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                          const uint64_t *sizes, size_t n, int dir, int cta_budget,
+                          void *stream);
+
+/* kvx_copy_batch with an explicit launch configuration (NULL = all table). */
+kvx_status kvx_copy_batch_ex(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                             const uint64_t *sizes, size_t n, int dir,
+                             const kvx_launch *launch, void *stream);
+
+/* ---- reusable descriptor buffers (pinned staging + device table) -------- */
+
+/* Create a buffer for up to max_chunks chunk records (1..KVX_MAX_CHUNKS) on
+ * the current device. Allocates device and pinned host memory (synchronous). */
+kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out);
+
+/* Validate, chunk and pack a batch into the buffer's pinned staging area and
+ * enqueue its upload on `stream`. Waits on the host only while the buffer's
+ * previous upload is still in flight. The caller orders this upload after any
+ * kvx_copy_uploaded of the same buffer that is still running on another
+ * stream (same stream: ordered already). Not allowed during capture. */
+kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
+                                  const uint64_t *dst_addrs, const uint64_t *sizes,
+                                  size_t n, int dir, void *stream);
+
+/* Launch the copy kernel over the uploaded table. No host work besides the
+ * launch: fixed shape, allowed inside CUDA graph capture. `cta_budget` as in
+ * kvx_copy_batch. */
+kvx_status kvx_copy_uploaded(kvx_desc_buf *buf, int cta_budget, void *stream);
+
+/* kvx_copy_uploaded with an explicit launch configuration (NULL = table). */
+kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *buf, const kvx_launch *launch, void *stream);
+
+/* Chunks and payload bytes of the last upload, and the launch configuration
+ * the table selected for it. Any output pointer may be NULL. */
+kvx_status kvx_desc_buf_info(const kvx_desc_buf *buf, size_t *n_chunks,
+                             uint64_t *payload_bytes, kvx_launch *selected);
+
+/* Wait for the buffer's last upload and last copy, then free it. */
+kvx_status kvx_desc_buf_destroy(kvx_desc_buf *buf);
+
+/* ---- host-only helpers (no CUDA call, no GPU needed) -------------------- */
+
+/* Validate a batch at `level` (0: arrays, dir, alignment, overflow, capacity;
+ * 1: + destination overlap; 2: + address kinds, which calls the CUDA
+ * runtime). Returns the status kvx_copy_batch would return before enqueuing. */
+kvx_status kvx_validate(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                        const uint64_t *sizes, size_t n, int dir, int level);
+
+/* The chunk table kvx would upload for a batch. With out == NULL only
+ * *n_chunks is set. KVX_ERR_CAPACITY when it needs more than max_out. */
+kvx_status kvx_plan_chunks(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                           const uint64_t *sizes, size_t n, kvx_chunk *out,
+                           size_t max_out, size_t *n_chunks);
+
+/* The calibrated launch configuration for a direction and mean chunk size. */
+kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *out);
+
+/* Process-wide validation level for kvx_copy_batch / kvx_upload_descriptors
+ * (0..2). Initial value: the KVX_VALIDATE environment variable, else 0. */
+kvx_status kvx_set_validate_level(int level);
+int kvx_get_validate_level(void);
+
+const char *kvx_status_string(int status);
+/* Message of the last non-OK status returned in the calling thread. */
+const char *kvx_last_error(void);
+int kvx_version(void); /* KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR */
+
+/* ---- device status, memory ---------------------------------------------- */
+
+/* Synchronise `stream`, then read and clear the device status word that
+ * kernels set when a bounded wait gives up. The word is shared by all
+ * streams of the device, so an error raised by a kernel on another stream
+ * may be reported here. KVX_OK, KVX_ERR_TIMEOUT, KVX_ERR_DEVICE_FAULT or
+ * KVX_ERR_CUDA. */
+kvx_status kvx_stream_check(void *stream);
+
+/* Mapped, portable pinned host memory (cudaHostAlloc). Fails with
+ * KVX_ERR_NOT_MAPPED if the device address differs from the host address
+ * (no unified addressing). Synchronous; not for the hot path. */
+kvx_status kvx_host_alloc(size_t bytes, void **out);
+kvx_status kvx_host_free(void *ptr);
+
+/* ---- baselines (same validation; not the engine) ------------------------ */
+
+/* The direct path the pages compare against: coalesce descriptors that
+ * continue the previous one in both source and destination, then one
+ * directional cudaMemcpyAsync per merged range (PegaFlow issue #408,
+ * §Relevant implementation, MemcpyBackend). *n_ranges (may be NULL) receives
+ * the number of memcpy calls issued. */
+kvx_status kvx_copy_batch_memcpy(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                                 const uint64_t *sizes, size_t n, int dir, void *stream,
+                                 size_t *n_ranges);
+
+/* One contiguous directional cudaMemcpyAsync: the roofline probe of the host
+ * link (PegaFlow issue #408, §Results: contiguous pinned-memory DMA). */
+kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int dir,
+                               void *stream);
+
+/* ---- self-test of the bounded device wait ------------------------------- */
+
+/* Launch one CTA that waits on an mbarrier nothing ever completes, with the
+ * same bounded wait the bulk kernel uses, limited to timeout_ns (1 ms..10 s).
+ * The kernel gives up, sets the timeout bit of the status word and returns;
+ * a following kvx_stream_check returns KVX_ERR_TIMEOUT. Faults nothing. */
+kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_H */

@@ -1,0 +1,243 @@
+"""The C ABI on the host, without a GPU: exports, chunk planning, validation.
+
+No call here launches GPU work; the only entry points called are the
+host-only ones (kvx_validate, kvx_plan_chunks, kvx_default_launch, the
+validation level, status strings) and error paths that return before any
+CUDA call.
+"""
+
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from expert_host_block_gb300 import build as kbuild
+from expert_host_block_gb300 import kvx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built():
+    kbuild.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvx_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_lists():
+    assert _declared() == sorted(kvx.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = kvx.lib()
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", kvx.LIB_PATH], capture_output=True, text=True).stdout
+    defined = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(_declared()) <= defined
+
+
+def test_version_and_status_strings():
+    assert kvx.kvx_version() == 1
+    names = [kvx.status_string(s) for s in range(10)]
+    assert names[0] == "KVX_OK" and names[7] == "KVX_ERR_TIMEOUT" and names[9] == "KVX_ERR_CAPTURE"
+    assert kvx.status_string(99) == "KVX_ERR_UNKNOWN"
+
+
+# ---- chunk planning --------------------------------------------------------
+
+def _apply(pool_dst, pool_src, so, do, sz):
+    oracle.copy_batch(pool_dst, pool_src, so, do, sz)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_chunk_table_moves_the_same_bytes(seed):
+    """Applying the chunk records gives the oracle's result for the descriptors."""
+    g = np.random.default_rng(seed)
+    pool = 24 << 20
+    src = g.integers(0, 256, pool, dtype=np.uint8)
+    dst0 = g.integers(0, 256, pool, dtype=np.uint8)
+    n = 200
+    slot = 96 * 1024
+    sizes = (8 * g.integers(0, 80 * 1024 // 8, n)).astype(np.uint64)
+    sizes[:5] = [0, 8, 16384, 16392, 16384 * 3]
+    so = (g.permutation(pool // slot)[:n] * slot + 8 * g.integers(0, 2, n)).astype(np.uint64)
+    do = (g.permutation(pool // slot)[:n] * slot + 8 * g.integers(0, 2, n)).astype(np.uint64)
+    base_s, base_d = 1 << 40, 1 << 41
+    t = kvx.kvx_plan_chunks(so + base_s, do + base_d, sizes)
+    assert t.size == int(sum(-(-int(z) // 16384) for z in sizes))
+    assert np.all(t["len"] <= kvx.KVX_CHUNK_BYTES) and np.all(t["len"] > 0)
+    # each chunk stays inside its descriptor, and chunk offsets line up
+    i = t["desc"].astype(np.int64)
+    assert np.all(t["src"] - (so[i] + base_s) == t["dst"] - (do[i] + base_d))
+    assert np.all(t["src"] - (so[i] + base_s) + t["len"] <= sizes[i])
+    assert np.all(t["reserved"] == 0)
+    want = dst0.copy()
+    _apply(want, src, so, do, sizes)
+    got = dst0.copy()
+    _apply(got, src, t["src"] - base_s, t["dst"] - base_d, t["len"].astype(np.uint64))
+    assert np.array_equal(got, want)
+
+
+def test_moe_chunk_count_closed_form(golden):
+    """1 MiB / 16 KiB + 128 KiB / 16 KiB + 1 + 512 KiB / 16 KiB + ceil(68 KiB / 16 KiB) + 1 = 111."""
+    rows = [int(x) for x in golden("moe_banks.txt")["row_bytes"]]
+    m = W.MoeGather()
+    b = m.next_call()
+    t = kvx.kvx_plan_chunks(b.src_off + (1 << 40), b.dst_off + (1 << 41), b.sizes)
+    assert 64 + 8 + 1 + 32 + 5 + 1 == 111
+    assert t.size == 32 * 111 == 3552
+    assert int(t["len"].astype(np.int64).sum()) == 32 * sum(rows)
+
+
+def test_plan_empty_and_zero_sizes():
+    assert kvx.kvx_plan_chunks([], [], []).size == 0
+    t = kvx.kvx_plan_chunks([0, 8], [0, 16], [0, 0])
+    assert t.size == 0
+
+
+# ---- validation ------------------------------------------------------------
+
+def _ok_batch():
+    return (np.array([1 << 20, 2 << 20], np.uint64), np.array([3 << 20, 4 << 20], np.uint64),
+            np.array([4096, 8], np.uint64))
+
+
+def test_validate_accepts_good_batch():
+    s, d, z = _ok_batch()
+    for level in (0, 1):
+        assert kvx.kvx_validate(s, d, z, None, kvx.KVX_H2D, level) == kvx.KVX_OK
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("size", 4100, kvx.KVX_ERR_ALIGN),
+    ("size", 12, kvx.KVX_ERR_ALIGN),
+    ("src", (1 << 20) + 4, kvx.KVX_ERR_ALIGN),
+    ("dst", (3 << 20) + 1, kvx.KVX_ERR_ALIGN),
+    ("src", 0, kvx.KVX_ERR_INVALID_ARG),
+    ("dst", 0, kvx.KVX_ERR_INVALID_ARG),
+    ("src", (1 << 64) - 8, kvx.KVX_ERR_INVALID_ARG),
+])
+def test_validate_rejects(field, value, status):
+    s, d, z = _ok_batch()
+    {"size": z, "src": s, "dst": d}[field][0] = value
+    assert kvx.kvx_validate(s, d, z, None, kvx.KVX_D2D, 0) == status
+    assert kvx.last_error()
+
+
+def test_validate_zero_size_ignores_addresses():
+    assert kvx.kvx_validate([0, 3], [0, 5], [0, 0], None, kvx.KVX_H2D, 1) == kvx.KVX_OK
+
+
+def test_validate_bad_dir_and_level():
+    s, d, z = _ok_batch()
+    assert kvx.kvx_validate(s, d, z, None, 3, 0) == kvx.KVX_ERR_INVALID_ARG
+    assert kvx.kvx_validate(s, d, z, None, -1, 0) == kvx.KVX_ERR_INVALID_ARG
+    assert kvx.kvx_validate(s, d, z, None, kvx.KVX_H2D, 3) == kvx.KVX_ERR_INVALID_ARG
+
+
+def test_validate_null_arrays():
+    L = kvx.lib()
+    assert L.kvx_validate(None, None, None, 4, 0, 0) == kvx.KVX_ERR_INVALID_ARG
+    assert L.kvx_validate(None, None, None, 0, 0, 0) == kvx.KVX_OK
+
+
+def test_validate_overlap_only_at_level_1():
+    s = np.array([1 << 20, 2 << 20], np.uint64)
+    d = np.array([3 << 20, (3 << 20) + 4088], np.uint64)  # second starts 8 bytes before the first ends
+    z = np.array([4096, 4096], np.uint64)
+    assert kvx.kvx_validate(s, d, z, None, kvx.KVX_D2D, 0) == kvx.KVX_OK
+    assert kvx.kvx_validate(s, d, z, None, kvx.KVX_D2D, 1) == kvx.KVX_ERR_OVERLAP
+    d2 = np.array([3 << 20, (3 << 20) + 4096], np.uint64)  # touching, not overlapping
+    assert kvx.kvx_validate(s, d2, z, None, kvx.KVX_D2D, 1) == kvx.KVX_OK
+    # a destination overlapping a source of the batch
+    s3 = np.array([(3 << 20) + 8, 2 << 20], np.uint64)  # inside the second destination
+    assert kvx.kvx_validate(s3, d2 - np.uint64(4096), z, None, kvx.KVX_D2D, 1) == kvx.KVX_ERR_OVERLAP
+
+
+def test_validate_overlap_matches_oracle_disjointness():
+    g = np.random.default_rng(3)
+    for _ in range(300):
+        n = int(g.integers(1, 7))
+        d = (8 * g.integers(1, 40, n)).astype(np.uint64) + np.uint64(1 << 30)
+        z = (8 * g.integers(0, 6, n)).astype(np.uint64)
+        s = (8 * g.integers(1, 40, n)).astype(np.uint64) + np.uint64(1 << 20)  # far from d
+        want = kvx.KVX_OK if oracle.ranges_disjoint(d, z) else kvx.KVX_ERR_OVERLAP
+        assert kvx.kvx_validate(s, d, z, None, kvx.KVX_D2D, 1) == want
+
+
+def test_capacity_limit():
+    # one descriptor of (KVX_MAX_CHUNKS + 1) * 16 KiB
+    z = np.array([(kvx.KVX_MAX_CHUNKS + 1) * kvx.KVX_CHUNK_BYTES], np.uint64)
+    assert kvx.kvx_validate([1 << 20], [1 << 40], z, None, kvx.KVX_D2D, 0) == kvx.KVX_ERR_CAPACITY
+    z = np.array([kvx.KVX_MAX_CHUNKS * kvx.KVX_CHUNK_BYTES], np.uint64)
+    assert kvx.kvx_validate([1 << 20], [1 << 40], z, None, kvx.KVX_D2D, 0) == kvx.KVX_OK
+
+
+def test_copy_batch_rejects_before_any_cuda_call():
+    s, d, z = _ok_batch()
+    z[1] = 12
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_copy_batch(s, d, z, None, kvx.KVX_H2D, 0, None)
+    assert e.value.status == kvx.KVX_ERR_ALIGN
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_copy_batch(s, d, z, None, kvx.KVX_H2D, -1, None)
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_copy_batch_memcpy(s, d, z, None, 7, None)
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+    # n == 0 is a no-op that needs no device
+    kvx.kvx_copy_batch([], [], [], None, kvx.KVX_H2D, 0, None)
+
+
+@pytest.mark.parametrize("launch", [
+    {"variant": 3}, {"threads": 1024}, {"threads": 96}, {"unroll": 3}, {"stages": 5},
+    {"store_policy": 3}, {"cta_budget": -2},
+])
+def test_copy_batch_ex_rejects_bad_launch(launch):
+    s, d, z = _ok_batch()
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_copy_batch_ex(s, d, z, None, kvx.KVX_D2D, launch, None)
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+
+
+def test_default_launch_table():
+    for dname in ("h2d", "d2h", "d2d"):
+        for mean in (8, 4096, 16384):
+            l = kvx.kvx_default_launch(dname, mean)
+            assert l["variant"] in (kvx.KVX_VARIANT_LDG, kvx.KVX_VARIANT_BULK)
+            assert l["cta_budget"] > 0 and l["threads"] in (128, 256, 512)
+            assert l["unroll"] in (2, 4, 8) and 2 <= l["stages"] <= 4
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_default_launch(5, 4096)
+
+
+def test_validate_level_setting():
+    kvx.kvx_set_validate_level(1)
+    assert kvx.kvx_get_validate_level() == 1
+    kvx.kvx_set_validate_level(0)
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_set_validate_level(3)
+
+
+@pytest.mark.parametrize("var,val", [("KVX_VARIANT", "tma"), ("KVX_VALIDATE", "yes"),
+                                     ("KVX_CTA_BUDGET", "-4"), ("KVX_CTA_BUDGET", "12x")])
+def test_unknown_env_values_are_errors(var, val):
+    code = ("from expert_host_block_gb300 import kvx\n"
+            "try:\n"
+            "    kvx.kvx_copy_batch([8], [16], [8], None, 0, 0, None)\n"
+            "except kvx.KvxError as e:\n"
+            "    print(e.status, e)\n")
+    env = dict(os.environ, **{var: val})
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    assert out.stdout.startswith(f"{kvx.KVX_ERR_INVALID_ARG} "), out.stdout + out.stderr
+    assert var in out.stdout

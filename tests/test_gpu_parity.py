@@ -1,0 +1,379 @@
+"""GPU parity: every copy through the C ABI is bit-exact against the oracle.
+
+Each test allocates the workload's pools, snapshots them, runs the batch on
+the GPU through libkvx.so and compares every byte of every pool (guard bands
+and canary included) with the oracle's result on the snapshots.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from expert_host_block_gb300 import kvx
+from harness import Pools, run_batch
+
+pytestmark = pytest.mark.gpu
+
+LDG = {"variant": "ldg"}
+BULK = {"variant": "bulk"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    from expert_host_block_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    kvx.kvx_set_validate_level(1)
+    yield
+    kvx.kvx_set_validate_level(0)
+
+
+def _one(pools, batch, **kw):
+    want = pools.expected([batch])
+    stream = torch.cuda.current_stream()
+    run_batch(pools, batch, stream=stream, **kw)
+    kvx.kvx_stream_check(stream)
+    pools.assert_equal(want)
+
+
+# ---- config: tiny H2D (1,024 x 4 KiB), full size ---------------------------
+
+@pytest.mark.parametrize("launch", [None, LDG, BULK,
+                                    {"variant": "ldg", "cta_budget": 1},
+                                    {"variant": "ldg", "cta_budget": 4},
+                                    {"variant": "ldg", "cta_budget": 8},
+                                    {"variant": "ldg", "cta_budget": 16},
+                                    {"variant": "ldg", "cta_budget": 32},
+                                    {"variant": "ldg", "cta_budget": 100000},
+                                    {"variant": "bulk", "cta_budget": 1},
+                                    {"variant": "bulk", "cta_budget": 4},
+                                    {"variant": "bulk", "cta_budget": 32, "stages": 2},
+                                    {"variant": "bulk", "cta_budget": 8, "stages": 4}])
+def test_tiny_h2d(launch):
+    w = W.tiny_h2d()
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0], launch=launch)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("threads", [128, 256, 512])
+@pytest.mark.parametrize("unroll", [2, 4, 8])
+@pytest.mark.parametrize("policy", [0, 1, 2])
+def test_ldg_launch_shapes(threads, unroll, policy):
+    w = W.sweep_cell(28, 300, "h2d", odd_tails=True)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0], launch={"variant": "ldg", "threads": threads, "unroll": unroll,
+                                      "store_policy": policy, "cta_budget": 7})
+    finally:
+        p.close()
+
+
+# ---- config: KV burst, 16,384 x 4 KiB per direction, H2D || D2H, full size ---
+
+@pytest.mark.parametrize("launch", [None, BULK])
+def test_kv_burst_bidirectional(launch):
+    w = W.kv_burst(n_sets=1)
+    p = Pools(w.pools)
+    try:
+        h2d, d2h = w.batches[0]
+        want = p.expected([h2d, d2h])
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        run_batch(p, h2d, stream=s1, launch=launch)
+        run_batch(p, d2h, stream=s2, launch=launch)
+        kvx.kvx_stream_check(s1)
+        kvx.kvx_stream_check(s2)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+def test_kv_burst_many_sets_ring_reuse():
+    """More calls than staging slots, on two streams: every slot is reused."""
+    w = W.kv_burst(n_sets=12, n_per_dir=2048, pool_bytes=256 * W.MIB)
+    p = Pools(w.pools)
+    try:
+        want = p.expected([b for pair in w.batches for b in pair])
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        for h2d, d2h in w.batches:
+            run_batch(p, h2d, stream=s1)
+            run_batch(p, d2h, stream=s2)
+        kvx.kvx_stream_check(s1)
+        kvx.kvx_stream_check(s2)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+# ---- config: size / count sweep ----------------------------------------------
+
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+@pytest.mark.parametrize("odd", [False, True])
+@pytest.mark.parametrize("size_kib", W.SWEEP_SIZES_KIB)
+@pytest.mark.parametrize("launch", [LDG, BULK])
+def test_sweep_cells(direction, odd, size_kib, launch):
+    w = W.sweep_cell(size_kib, 256, direction, odd_tails=odd)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0], launch=launch)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+@pytest.mark.parametrize("n", [16, 4096, 65536])
+def test_sweep_counts_default_launch(direction, n):
+    w = W.sweep_cell(4, n, direction, odd_tails=False)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0])
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("direction", ["h2d", "d2d"])
+def test_sweep_full_size_cell(direction):
+    """The largest sweep cell: 8,192 x 64 KiB = 512 MiB."""
+    w = W.sweep_cell(64, 65_536, direction, odd_tails=False)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0])
+    finally:
+        p.close()
+
+
+# ---- config: MoE expert-miss gather, full size -----------------------------------
+
+@pytest.mark.parametrize("launch", [None, LDG, BULK])
+def test_moe_gather(launch):
+    m = W.MoeGather()
+    p = Pools(m.pools)
+    try:
+        calls = [m.next_call() for _ in range(3)]
+        want = p.expected(calls)
+        stream = torch.cuda.current_stream()
+        for b in calls:
+            run_batch(p, b, stream=stream, launch=launch)
+        kvx.kvx_stream_check(stream)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+# ---- edge cases -------------------------------------------------------------------
+
+def _pools_small(where_src="host", where_dst="device", body=1 << 20):
+    return Pools({"src": W.PoolSpec("src", where_src, body, "random", (90,)),
+                  "dst": W.PoolSpec("dst", where_dst, body, "canary")})
+
+
+def _batch(so, do, sz, direction):
+    u = lambda a: np.asarray(a, dtype=np.uint64)
+    return W.Batch("src", "dst", u(so), u(do), u(sz), direction)
+
+
+@pytest.mark.parametrize("launch", [LDG, BULK])
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+def test_phase_combinations(direction, launch):
+    """Sizes 8..40 and around the chunk size at every (src mod 16, dst mod 16) pair."""
+    ws = "host" if direction == "h2d" else "device"
+    wd = "host" if direction == "d2h" else "device"
+    p = _pools_small(ws, wd)
+    so, do, sz = [], [], []
+    slot = 40 * 1024
+    k = 0
+    for size in (8, 16, 24, 32, 40, 16376, 16384, 16392, 32768 + 8):
+        for sp in (0, 8):
+            for dp in (0, 8):
+                so.append(k * slot + sp)
+                do.append(k * slot + dp)
+                sz.append(size)
+                k += 1
+    try:
+        _one(p, _batch(so, do, sz, direction), launch=launch)
+    finally:
+        p.close()
+
+
+def test_empty_and_zero_size_batches():
+    p = _pools_small()
+    try:
+        want = p.expected([])
+        kvx.kvx_copy_batch([], [], [], None, "h2d", 0, None)
+        base = p.base("src")
+        kvx.kvx_copy_batch([base, 0], [p.base("dst"), 0], [0, 0], None, "h2d", 0, None)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("launch", [LDG, BULK])
+def test_single_large_descriptor(launch):
+    """One 64 MiB descriptor (4,096 chunks) and one 8-byte descriptor."""
+    p = _pools_small("device", "device", body=80 * W.MIB)
+    try:
+        _one(p, _batch([0, 70 * W.MIB], [8 * W.MIB, 75 * W.MIB], [64 * W.MIB, 8], "d2d"), launch=launch)
+    finally:
+        p.close()
+
+
+def test_same_pool_d2d():
+    p = Pools({"pool": W.PoolSpec("pool", "device", 4 * W.MIB, "random", (91,))})
+    try:
+        b = W.Batch("pool", "pool", np.arange(0, 64, dtype=np.uint64) * 16384,
+                    np.arange(64, 128, dtype=np.uint64) * 16384 + 8, np.full(64, 16376, np.uint64), "d2d")
+        _one(p, b)
+    finally:
+        p.close()
+
+
+# ---- descriptor buffers, graph capture ---------------------------------------------
+
+@pytest.mark.parametrize("variant", ["ldg", "bulk"])
+def test_desc_buf_upload_and_replay(variant):
+    w = W.kv_burst(n_sets=2, n_per_dir=4096, pool_bytes=128 * W.MIB)
+    p = Pools(w.pools)
+    buf = kvx.DescBuf(8192)
+    try:
+        stream = torch.cuda.current_stream()
+        h2d_a, _ = w.batches[0]
+        h2d_b, _ = w.batches[1]
+        want = p.expected([h2d_a])
+        buf.upload(*p.addrs(h2d_a), "h2d", stream)
+        n, payload, sel = buf.info()
+        assert n == 4096 and payload == 4096 * 4096
+        buf.copy(stream=stream, launch={"variant": variant})
+        buf.copy(stream=stream, launch={"variant": variant, "cta_budget": 3})  # idempotent replay
+        kvx.kvx_stream_check(stream)
+        p.assert_equal(want)
+        want = p.expected([h2d_b])
+        buf.upload(*p.addrs(h2d_b), "h2d", stream)
+        buf.copy(stream=stream, launch={"variant": variant})
+        kvx.kvx_stream_check(stream)
+        p.assert_equal(want)
+    finally:
+        buf.close()
+        p.close()
+
+
+def test_desc_buf_capacity():
+    buf = kvx.DescBuf(4)
+    try:
+        with pytest.raises(kvx.KvxError) as e:
+            buf.upload([1 << 20], [1 << 30], [5 * 16384], "d2d")
+        assert e.value.status == kvx.KVX_ERR_CAPACITY
+    finally:
+        buf.close()
+
+
+def test_graph_capture_of_uploaded_copy():
+    w = W.tiny_h2d()
+    p = Pools(w.pools)
+    buf = kvx.DescBuf(1024)
+    try:
+        (b,) = w.batches
+        want = p.expected([b])
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            buf.upload(*p.addrs(b), "h2d", s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            buf.copy(stream=s)
+            with pytest.raises(kvx.KvxError) as e:  # the host-staging path refuses capture
+                run_batch(p, b, stream=s)
+            assert e.value.status == kvx.KVX_ERR_CAPTURE
+        # capture itself ran nothing: the destination is still all canary
+        torch.cuda.synchronize()
+        assert np.all(p.snapshot("dev") == W.CANARY)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        buf.close()
+        p.close()
+
+
+# ---- validation with real pointers, baselines, bounded wait ---------------------
+
+def test_validate_level2_address_kinds():
+    p = _pools_small()
+    try:
+        hs, dd = p.base("src"), p.base("dst")
+        assert kvx.kvx_validate([hs], [dd], [4096], None, "h2d", 2) == kvx.KVX_OK
+        assert kvx.kvx_validate([dd], [hs], [4096], None, "h2d", 2) == kvx.KVX_ERR_NOT_MAPPED
+        assert kvx.kvx_validate([hs], [dd], [4096], None, "d2d", 2) == kvx.KVX_ERR_NOT_MAPPED
+        assert kvx.kvx_validate([dd], [hs], [4096], None, "d2h", 2) == kvx.KVX_OK
+    finally:
+        p.close()
+
+
+def test_overlap_rejected_and_nothing_enqueued():
+    p = _pools_small()
+    try:
+        want = p.expected([])
+        hs, dd = p.base("src"), p.base("dst")
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_copy_batch([hs, hs + 8192], [dd, dd + 4088], [4096, 4096], None, "h2d", 0, None)
+        assert e.value.status == kvx.KVX_ERR_OVERLAP
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+def test_memcpy_baseline_parity(direction):
+    w = W.sweep_cell(8, 256, direction, odd_tails=True)
+    p = Pools(w.pools)
+    try:
+        (b,) = w.batches
+        want = p.expected([b])
+        s, d, z = p.addrs(b)
+        nr = kvx.kvx_copy_batch_memcpy(s, d, z, None, direction, None)
+        assert nr == b.n  # shuffled slots: nothing to coalesce
+        torch.cuda.synchronize()
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+def test_memcpy_baseline_coalesces_adjacent():
+    p = _pools_small()
+    try:
+        so = np.arange(16, dtype=np.uint64) * 4096
+        b = _batch(so, so + np.uint64(65536), np.full(16, 4096), "h2d")
+        want = p.expected([b])
+        s, d, z = p.addrs(b)
+        assert kvx.kvx_copy_batch_memcpy(s, d, z, None, "h2d", None) == 1
+        torch.cuda.synchronize()
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    stream = torch.cuda.current_stream()
+    kvx.kvx_stream_check(stream)  # clear
+    kvx.kvx_selftest_wait_timeout(50_000_000, stream)  # 50 ms
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_stream_check(stream)
+    assert e.value.status == kvx.KVX_ERR_TIMEOUT
+    kvx.kvx_stream_check(stream)  # the bit was cleared
+    # the context is still usable
+    w = W.tiny_h2d()
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0])
+    finally:
+        p.close()
