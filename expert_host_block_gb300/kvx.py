@@ -53,6 +53,8 @@ EXPORTS = (
     "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version",
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
     "kvx_copy_contiguous", "kvx_selftest_wait_timeout",
+    # include/kvx_standin.h
+    "kvx_standin_gemv_bf16",
 )
 
 
@@ -109,6 +111,7 @@ def _load():
         "kvx_copy_batch_memcpy": ([_vp, _vp, _vp, _sz, _int, _vp, ctypes.POINTER(_sz)], _int),
         "kvx_copy_contiguous": ([_u64, _u64, _u64, _int, _vp], _int),
         "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
+        "kvx_standin_gemv_bf16": ([_u64, _u64, _u64, _u64, ctypes.c_uint32, _int, _vp], _int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -366,3 +369,13 @@ def kvx_copy_contiguous(dst: int, src: int, nbytes: int, dir, stream=None) -> No
 
 def kvx_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(_load().kvx_selftest_wait_timeout(int(timeout_ns), _stream(stream)))
+
+
+# ---- decode stand-in (include/kvx_standin.h) -------------------------------
+
+def kvx_standin_gemv_bf16(W: int, x: int, y: int, rows: int, cols: int, ctas: int = 0, stream=None) -> None:
+    """y = W @ x with W (rows x cols) and x in bf16, fp32 accumulation; device addresses."""
+    st = _load().kvx_standin_gemv_bf16(int(W), int(x), int(y), int(rows), int(cols), int(ctas),
+                                       _stream(stream))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_standin_gemv_bf16: bad arguments or launch failure")

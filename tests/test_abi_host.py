@@ -6,6 +6,7 @@ validation level, status strings) and error paths that return before any
 CUDA call.
 """
 
+import glob
 import os
 import re
 import subprocess
@@ -28,9 +29,11 @@ def _built():
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "kvx.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kvx_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(kvx_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_what_binding_lists():

@@ -185,7 +185,7 @@ def test_phase_combinations(direction, launch):
     """Sizes 8..40 and around the chunk size at every (src mod 16, dst mod 16) pair."""
     ws = "host" if direction == "h2d" else "device"
     wd = "host" if direction == "d2h" else "device"
-    p = _pools_small(ws, wd)
+    p = _pools_small(ws, wd, body=2 * W.MIB)
     so, do, sz = [], [], []
     slot = 40 * 1024
     k = 0
