@@ -1,6 +1,9 @@
 // bf16 GEMV decode stand-in for the interference measurement (see kvx_standin.h).
 //
-// One warp per row, persistent grid. A row of 2,560 bf16 is 320 16-byte words:
+// One warp per row, grid-stride over rows. The default grid gives each warp
+// about 8 rows, so CTAs come and go like a real decode kernel's and the
+// scheduler can place them around other kernels' CTAs. A row of 2,560 bf16 is
+// 320 16-byte words:
 // each lane issues its 10 loads back to back (5 KiB per warp in flight), then
 // multiplies with x, kept in shared memory as fp32, and the warp reduces with
 // shuffles. The weights are read once with no reuse, so the loads bypass L1.
@@ -27,7 +30,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void __launch_bounds__(512) kvx_standin_gemv_kernel(const uint4 *__restrict__ W,
+__global__ void __launch_bounds__(256) kvx_standin_gemv_kernel(const uint4 *__restrict__ W,
                                                                const uint16_t *__restrict__ x,
                                                                float *__restrict__ y, uint64_t rows,
                                                                uint32_t cols)
@@ -81,14 +84,11 @@ extern "C" kvx_status kvx_standin_gemv_bf16(uint64_t W, uint64_t x, uint64_t y, 
         return KVX_ERR_INVALID_ARG;
     if ((W | x | y) & 15u)
         return KVX_ERR_ALIGN;
-    if (ctas == 0) {
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return KVX_ERR_CUDA;
-        ctas = sms;  // 109 registers x 512 threads: one CTA per SM
+    if (ctas == 0) {  // 8 warps per CTA, about 8 rows per warp
+        const uint64_t want = (rows + 63) / 64;
+        ctas = (int)(want < (1u << 30) ? want : (1u << 30));
     }
-    kvx_standin_gemv_kernel<<<ctas, 512, cols * sizeof(float), static_cast<cudaStream_t>(stream)>>>(
+    kvx_standin_gemv_kernel<<<ctas, 256, cols * sizeof(float), static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const uint4 *>(W), reinterpret_cast<const uint16_t *>(x),
         reinterpret_cast<float *>(y), rows, cols);
     return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;

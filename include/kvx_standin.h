@@ -26,7 +26,7 @@ extern "C" {
 /* Enqueue the GEMV on `stream` (a cudaStream_t). W: rows x cols bf16 device
  * array, 16-byte aligned; x: cols bf16 device array; y: rows fp32 device
  * array. cols must be a multiple of 256 and at most 4096; rows >= 1.
- * `ctas` = grid size (0 = one CTA of 512 threads per SM). Returns
+ * `ctas` = grid size of 256-thread CTAs (0 = about 8 rows per warp). Returns
  * KVX_ERR_INVALID_ARG / KVX_ERR_ALIGN for bad arguments (nothing enqueued) and
  * KVX_ERR_CUDA if the launch fails. */
 kvx_status kvx_standin_gemv_bf16(uint64_t W, uint64_t x, uint64_t y, uint64_t rows, uint32_t cols,
