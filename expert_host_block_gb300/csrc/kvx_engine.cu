@@ -263,9 +263,15 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
 // ---------------------------------------------------------------------------
 // launch table
 // ---------------------------------------------------------------------------
-// Rows by direction and mean chunk size. The host-link rows target bytes in
-// flight rather than threads (FreeToken issue #751, §Measured impact and
-// §Proposal: the optimum follows bytes in flight); the D2D row fills the GPU.
+// Rows by direction and mean chunk size, from the calibration sweep on a
+// GB300 (NVLink-C2C host link). The host-link rows target bytes in flight
+// rather than threads (FreeToken issue #751, §Measured impact and §Proposal:
+// the optimum follows bytes in flight): one direction alone saturates the
+// link at about 512 KiB in flight (8 CTAs x 512 threads x 8 x 16 B), and H2D
+// and D2H running together need about 1.5 MiB per direction (24 CTAs). The
+// LDG variant reached the link peak in every measured size class with fewer
+// CTAs than the bulk ring, so every row picks it. D2D fills the GPU: one
+// 512-thread CTA per SM (107 registers a thread leave room for one).
 struct TableRow {
     int dir;
     uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
@@ -273,9 +279,9 @@ struct TableRow {
 };
 
 const TableRow kTable[] = {
-    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
-    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 304, 256, 8, 3, 0}},
+    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 24, 512, 8, 3, 0}},
+    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 24, 512, 8, 3, 0}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0}},
 };
 
 kvx_launch table_launch(int dir, uint64_t mean_chunk)
