@@ -863,3 +863,75 @@ kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kvx_copy_batch_noalloc: the same batch copy with no allocation at call time
+// ---------------------------------------------------------------------------
+namespace {
+
+// The chunk table of kvx_copy_batch_noalloc, in the library's own device
+// memory: every GPU that loads the library holds these 2 MiB until exit.
+static __device__ __align__(256) kvx_chunk g_noalloc_table[KVX_NOALLOC_MAX_CHUNKS];
+
+// Host side of the table. It is packed here and copied with a pageable
+// cudaMemcpyAsync, which stages the bytes before it returns, so the array can
+// be refilled as soon as the call returns.
+kvx_chunk g_noalloc_stage[KVX_NOALLOC_MAX_CHUNKS];
+
+// Serialises callers from pack to launch: the host array has one owner at a
+// time, and calls on one stream enqueue upload and kernel back to back.
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_table per device. In host code the symbol is
+// only a host-side stand-in, so the address comes from cudaGetSymbolAddress
+// with the device current (first call on each device).
+kvx_chunk *g_noalloc_dev[kMaxDevices];
+
+}  // namespace
+
+extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t *dst,
+                                             const uint64_t *sizes, size_t n, int dir, int cta_budget,
+                                             void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (cta_budget < 0)
+        return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", cta_budget);
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    uint64_t chunks = 0, payload = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    if (st != KVX_OK)
+        return st;
+    if (chunks > KVX_NOALLOC_MAX_CHUNKS)
+        return fail(KVX_ERR_CAPACITY,
+                    "batch needs %llu chunks; kvx_copy_batch_noalloc holds at most KVX_NOALLOC_MAX_CHUNKS "
+                    "(%u)", (unsigned long long)chunks, KVX_NOALLOC_MAX_CHUNKS);
+    kvx_launch want{};
+    want.cta_budget = cta_budget;
+    Launch l;
+    st = resolve(dir, chunks ? payload / chunks : 0, &want, &l);
+    if (st != KVX_OK)
+        return st;
+    if (chunks == 0)
+        return KVX_OK;
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_dev[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_table);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk table)");
+        g_noalloc_dev[dev] = static_cast<kvx_chunk *>(p);
+    }
+    pack(src, dst, sizes, n, g_noalloc_stage);
+    KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage, (size_t)chunks * sizeof(kvx_chunk),
+                                 cudaMemcpyHostToDevice, stream));
+    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy kernel launch");
+    return KVX_OK;
+}

@@ -52,7 +52,7 @@ EXPORTS = (
     "kvx_validate", "kvx_plan_chunks", "kvx_default_launch", "kvx_set_validate_level",
     "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version",
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
-    "kvx_copy_contiguous", "kvx_selftest_wait_timeout",
+    "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
@@ -111,6 +111,7 @@ def _load():
         "kvx_copy_batch_memcpy": ([_vp, _vp, _vp, _sz, _int, _vp, ctypes.POINTER(_sz)], _int),
         "kvx_copy_contiguous": ([_u64, _u64, _u64, _int, _vp], _int),
         "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
+        "kvx_copy_batch_noalloc": ([_vp, _vp, _vp, _sz, _int, _int, _vp], _int),
         "kvx_standin_gemv_bf16": ([_u64, _u64, _u64, _u64, ctypes.c_uint32, _int, _vp], _int),
     }
     for name, (args, res) in sig.items():
@@ -365,6 +366,20 @@ def kvx_copy_batch_memcpy(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, stre
 
 def kvx_copy_contiguous(dst: int, src: int, nbytes: int, dir, stream=None) -> None:
     _check(_load().kvx_copy_contiguous(int(dst), int(src), int(nbytes), _dir(dir), _stream(stream)))
+
+
+KVX_NOALLOC_MAX_CHUNKS = 65536
+
+
+def kvx_copy_batch_noalloc(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, cta_budget=0, stream=None) -> None:
+    """kvx_copy_batch for callers that cannot allocate at copy time (fixed 2 MiB device table).
+
+    At most KVX_NOALLOC_MAX_CHUNKS chunks per call; calls on different streams
+    that overlap on the GPU share the table and race (see include/kvx.h).
+    """
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    _check(_load().kvx_copy_batch_noalloc(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                          int(cta_budget), _stream(stream)))
 
 
 def kvx_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

@@ -226,6 +226,43 @@ kvx_status kvx_copy_batch_memcpy(const uint64_t *src_addrs, const uint64_t *dst_
 kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int dir,
                                void *stream);
 
+/* ---- a batch copy that allocates nothing -------------------------------- */
+
+/* The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate memory at copy time. kvx_copy_batch allocates its
+ * staging ring lazily (cudaHostAlloc and cudaMalloc on a slot's first use,
+ * and again, with a device-synchronising cudaFree, when a bigger batch makes a
+ * slot grow). Some callers cannot accept that: a serving engine that reserves
+ * almost all HBM for its KV cache at start-up leaves later cudaMalloc calls to
+ * fail, and a decode loop with a fixed per-step budget cannot absorb an
+ * allocation or a device-wide synchronisation in the middle of a step.
+ *
+ * kvx_copy_batch_noalloc takes the same arguments and moves the same bytes as
+ * kvx_copy_batch, with the same validation and error rules, but calls no
+ * cudaMalloc, cudaFree, cudaHostAlloc or other allocating routine. Its chunk
+ * table lives in a fixed array of KVX_NOALLOC_MAX_CHUNKS records (2 MiB) in the
+ * library's own device memory, which every GPU that loads the library holds
+ * until the process exits; the records are packed into a fixed host array of
+ * the same size and copied with one cudaMemcpyAsync from that (pageable)
+ * array, which the runtime stages before returning.
+ *   - A batch that needs more than KVX_NOALLOC_MAX_CHUNKS chunks returns
+ *     KVX_ERR_CAPACITY and enqueues nothing.
+ *   - The first call on a device looks up the device address of the array
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one array per device. Calls from several host
+ *     threads are serialised until their copy is enqueued, so calls on one
+ *     stream are safe; calls on different streams whose copies overlap on the
+ *     GPU race on the array and may copy wrong bytes. Order them (one stream,
+ *     or events) when they may overlap.
+ *   - Nothing in the array has to start at zero: each call writes every record
+ *     its kernel reads. */
+#define KVX_NOALLOC_MAX_CHUNKS 65536u
+
+kvx_status kvx_copy_batch_noalloc(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                                  const uint64_t *sizes, size_t n, int dir, int cta_budget,
+                                  void *stream);
+
 /* ---- self-test of the bounded device wait ------------------------------- */
 
 /* Launch one CTA that waits on an mbarrier nothing ever completes, with the

@@ -1,0 +1,93 @@
+"""kvx_copy_batch_noalloc gives the same bytes as kvx_copy_batch, two calls in a row.
+
+Who needs it: callers that cannot let a copy allocate memory. A serving engine
+that reserves nearly all HBM for its KV cache at start-up makes any later
+cudaMalloc fail, and a decode loop with a fixed per-step time budget cannot
+absorb an allocation, or the device-wide synchronisation of a cudaFree, in the
+middle of a step. kvx_copy_batch allocates its staging ring lazily, so those
+callers use kvx_copy_batch_noalloc, whose chunk table is a fixed 2 MiB array
+in the library's own device memory.
+
+What is checked: the same two batches (a KV-style 4 KiB batch, then an odd-tail
+batch that needs fewer chunks, so the second call runs over a table still
+holding the first call's tail) go once through kvx_copy_batch into one
+destination pool and once through kvx_copy_batch_noalloc into an identical
+pool; the two pools must match byte for byte (the bit-exact tolerance of every
+copy test here), and both must match the oracle. A batch one chunk too large
+is refused before anything is enqueued.
+
+This file sorts last so that a run stopping at its first failure has run every
+other test first; it also passes alone in a fresh process.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from expert_host_block_gb300 import kvx
+from harness import Pools
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    from expert_host_block_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def _batches():
+    kv = W.kv_burst(n_sets=1, n_per_dir=4096, pool_bytes=64 * W.MIB)
+    first = kv.batches[0][0]                       # 4,096 x 4 KiB, host -> device
+    odd = W.sweep_cell(28, 300, "h2d", odd_tails=True).batches[0]   # 300 odd-tail descriptors
+    return first, odd
+
+
+def test_noalloc_matches_copy_batch_two_calls_in_a_row():
+    first, odd = _batches()
+    body = 64 * W.MIB
+    specs = {
+        "src": W.PoolSpec("src", "host", body, "random", (77,)),
+        "dst_ref": W.PoolSpec("dst_ref", "device", body, "canary"),
+        "dst_na": W.PoolSpec("dst_na", "device", body, "canary"),
+    }
+    p = Pools(specs)
+    try:
+        def addrs(b, dst):
+            return (b.src_off + np.uint64(p.base("src")), b.dst_off + np.uint64(p.base(dst)), b.sizes)
+
+        calls = [W.Batch("src", "dst_na", b.src_off, b.dst_off, b.sizes, "h2d") for b in (first, odd)]
+        want = p.expected(calls)["dst_na"]
+        stream = torch.cuda.current_stream()
+        for b in (first, odd):
+            kvx.kvx_copy_batch(*addrs(b, "dst_ref"), None, "h2d", 0, stream)
+        for b in (first, odd):                     # two calls in a row on one stream
+            kvx.kvx_copy_batch_noalloc(*addrs(b, "dst_na"), None, "h2d", 0, stream)
+        kvx.kvx_stream_check(stream)
+        ref, got = p.snapshot("dst_ref"), p.snapshot("dst_na")
+        assert np.array_equal(got, ref), f"{int(np.count_nonzero(got != ref))} bytes differ from kvx_copy_batch"
+        assert np.array_equal(got, want), "differs from the oracle"
+    finally:
+        p.close()
+
+
+def test_noalloc_refuses_more_than_its_table():
+    p = Pools({"src": W.PoolSpec("src", "device", 4 * W.MIB, "random", (78,)),
+               "dst": W.PoolSpec("dst", "device", 4 * W.MIB, "canary")})
+    try:
+        before = p.snapshot("dst")
+        n = kvx.KVX_NOALLOC_MAX_CHUNKS + 1        # 8-byte descriptors: one chunk each
+        s = np.full(n, p.base("src"), dtype=np.uint64) + (np.arange(n, dtype=np.uint64) % 1024) * np.uint64(8)
+        d = np.uint64(p.base("dst")) + np.arange(n, dtype=np.uint64) * np.uint64(8)
+        z = np.full(n, 8, dtype=np.uint64)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_copy_batch_noalloc(s, d, z, None, "d2d", 0, None)
+        assert e.value.status == kvx.KVX_ERR_CAPACITY
+        torch.cuda.synchronize()
+        assert np.array_equal(p.snapshot("dst"), before)
+    finally:
+        p.close()
