@@ -129,7 +129,7 @@ kvx_status check_env()
 // ---------------------------------------------------------------------------
 inline uint64_t chunks_of(uint64_t size)
 {
-    return (size + KVX_CHUNK_BYTES - 1) / KVX_CHUNK_BYTES;
+    return size / KVX_CHUNK_BYTES + (size % KVX_CHUNK_BYTES != 0);  // no overflow near 2^64
 }
 
 struct Range {
@@ -192,19 +192,41 @@ kvx_status check_kinds(const uint64_t *src, const uint64_t *dst, const uint64_t 
     return KVX_OK;
 }
 
-// Validate and count chunks and payload bytes.
+// Validate; count chunks and payload bytes, and find the longest chunk.
 kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
-                    int dir, int level, uint64_t *n_chunks, uint64_t *payload)
+                    int dir, int level, uint64_t *n_chunks, uint64_t *payload,
+                    uint32_t *max_chunk = nullptr)
 {
     if (dir < KVX_H2D || dir > KVX_D2D)
         return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
     if (level < 0 || level > 2)
         return fail(KVX_ERR_INVALID_ARG, "validation level %d is not 0, 1 or 2", level);
-    uint64_t chunks = 0, bytes = 0;
+    uint64_t chunks = 0, bytes = 0, longest = 0;
     if (n) {
         if (!src || !dst || !sizes)
             return fail(KVX_ERR_INVALID_ARG, "null descriptor array with n = %zu", n);
+        // One branch-free pass over every descriptor; the exact loop below runs
+        // only when this pass saw a problem, to name the first bad descriptor.
+        static_assert(KVX_CHUNK_BYTES == (1u << 14), "chunk count uses a shift");
+        constexpr uint64_t kHuge = 1ull << 40;  // one such descriptor exceeds KVX_MAX_CHUNKS
+        uint64_t bad = 0;
         for (size_t i = 0; i < n; ++i) {
+            const uint64_t z = sizes[i], s = src[i], d = dst[i];
+            const uint64_t live = z ? ~0ull : 0ull;
+            bad |= live & (((s | d | z) & 7u) |
+                           ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d) | (z > kHuge)) << 3));
+            chunks += (z >> 14) + ((z & (KVX_CHUNK_BYTES - 1)) != 0);
+            bytes += z;
+            longest = z > longest ? z : longest;
+        }
+        if (!bad) {
+            if (chunks > KVX_MAX_CHUNKS)
+                return fail(KVX_ERR_CAPACITY, "batch needs more than KVX_MAX_CHUNKS (%u) chunks",
+                            KVX_MAX_CHUNKS);
+        } else {
+            chunks = bytes = longest = 0;
+        }
+        for (size_t i = 0; bad && i < n; ++i) {
             const uint64_t z = sizes[i];
             if (!z)
                 continue;
@@ -217,8 +239,13 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
                             (unsigned long long)s, (unsigned long long)d, (unsigned long long)z);
             if (s + z < s || d + z < d)
                 return fail(KVX_ERR_INVALID_ARG, "descriptor %zu: range wraps the address space", i);
+            if (z > kHuge)
+                return fail(KVX_ERR_CAPACITY, "descriptor %zu: %llu bytes exceed KVX_MAX_CHUNKS chunks", i,
+                            (unsigned long long)z);
             chunks += chunks_of(z);
             bytes += z;
+            if (z > longest)
+                longest = z;
             if (chunks > KVX_MAX_CHUNKS)
                 return fail(KVX_ERR_CAPACITY, "batch needs more than KVX_MAX_CHUNKS (%u) chunks",
                             KVX_MAX_CHUNKS);
@@ -238,6 +265,8 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
         *n_chunks = chunks;
     if (payload)
         *payload = bytes;
+    if (max_chunk)
+        *max_chunk = (uint32_t)std::min<uint64_t>(longest, KVX_CHUNK_BYTES);
     return KVX_OK;
 }
 
@@ -453,6 +482,7 @@ struct kvx_desc_buf {
     bool upload_recorded = false;
     bool use_recorded = false;
     uint32_t n_chunks = 0;
+    uint32_t max_chunk = 0;
     uint64_t payload = 0;
     int dir = KVX_H2D;
     kvx_launch selected{};
@@ -536,7 +566,8 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     if (st != KVX_OK)
         return st;
     uint64_t chunks = 0, payload = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    uint32_t max_chunk = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
     if (st != KVX_OK)
         return st;
     Launch l;
@@ -565,7 +596,7 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
         ring_release(dev, s, stream, false);
         return cuda_fail(e, "cudaMemcpyAsync(chunk table)");
     }
-    e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, stream);
+    e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, max_chunk, stream);
     ring_release(dev, s, stream, true);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
@@ -627,7 +658,8 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     if (st != KVX_OK)
         return st;
     uint64_t chunks = 0, payload = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    uint32_t max_chunk = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
     if (st != KVX_OK)
         return st;
     if (chunks > b->cap)
@@ -655,6 +687,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     KVX_CUDA_TRY(cudaEventRecord(b->upload_done, stream));
     b->upload_recorded = true;
     b->n_chunks = (uint32_t)chunks;
+    b->max_chunk = max_chunk;
     b->payload = payload;
     b->dir = dir;
     b->selected = {l.variant, l.ctas, l.threads, l.unroll, l.stages, l.store_policy};
@@ -697,7 +730,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
-    cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, stream);
+    cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     if (!cap) {
@@ -900,7 +933,8 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     if (st != KVX_OK)
         return st;
     uint64_t chunks = 0, payload = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload);
+    uint32_t max_chunk = 0;
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
     if (st != KVX_OK)
         return st;
     if (chunks > KVX_NOALLOC_MAX_CHUNKS)
@@ -930,7 +964,7 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     pack(src, dst, sizes, n, g_noalloc_stage);
     KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage, (size_t)chunks * sizeof(kvx_chunk),
                                  cudaMemcpyHostToDevice, stream));
-    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, stream);
+    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, max_chunk, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     return KVX_OK;

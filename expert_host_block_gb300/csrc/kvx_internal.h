@@ -30,12 +30,14 @@ struct Launch {
     int store_policy;  // LDG store cache policy
 };
 
-// Grid needed to give every CTA some work, for a chunk count and variant.
-int work_ctas(const Launch &l, uint32_t n_chunks);
+// Grid needed to give every CTA some work, for a chunk count, the longest
+// chunk and the variant.
+int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
 
-// Enqueue the copy kernel over a device-resident chunk table.
+// Enqueue the copy kernel over a device-resident chunk table. max_chunk_len is
+// the longest record's len (it sets the LDG kernel's passes per chunk).
 cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
-                        cudaStream_t stream);
+                        uint32_t max_chunk_len, cudaStream_t stream);
 
 // Enqueue a 1-thread kernel that moves the status word into *host_word
 // (mapped pinned) and clears it.

@@ -1,12 +1,13 @@
 // Copy kernels of kvx for sm_103a.
 //
 // Both variants walk the same device-resident table of 32-byte chunk records
-// ({src, dst, len <= 16 KiB, desc}) as a persistent grid: work unit c goes to
-// worker (c mod workers), where a worker is a warp (LDG) or a CTA (BULK).
-// Chunks are at most 16 KiB, so handing them out round-robin spreads the
-// batch's bytes evenly over the workers, whatever mix of descriptor sizes it
-// holds (FreeToken issue #751, §Problem in upstream today and §What we
-// changed: split the call's bytes, not its banks, over the CTAs).
+// ({src, dst, len <= 16 KiB, desc}) as a persistent grid: work unit u goes to
+// worker (u mod workers), where a worker is a warp (LDG, whose units are warp
+// passes of at most 512 * U bytes) or a CTA (BULK, whose units are chunks).
+// Units are small and of nearly equal size, so handing them out round-robin
+// spreads the batch's bytes evenly over the workers, whatever mix of
+// descriptor sizes it holds (FreeToken issue #751, §Problem in upstream today
+// and §What we changed: split the call's bytes, not its banks, over the CTAs).
 //
 // LDG variant: every lane moves 16-byte words, `U` loads in flight per lane
 // before the matching stores (the pages' LDG kernel keeps one 16-byte load in
@@ -84,66 +85,91 @@ __device__ __forceinline__ void st8(unsigned char *p, uint2 v)
         asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// ---- one chunk, moved by one warp ---------------------------------------
+// ---- one warp pass over part of a chunk --------------------------------------
+//
+// A pass moves up to 512 * U bytes of one chunk: U 16-byte words per lane
+// (or 2U 8-byte words when source and destination differ in phase mod 16).
+// Pass k of a chunk covers body words [k * 32U, (k + 1) * 32U); pass 0 also
+// moves the 8-byte head and tail. All loads of a pass are issued before any
+// of its stores, so a lane has U (or 2U, plus an edge word) loads in flight.
+
+template <int U>
+struct PassBytes {
+    static constexpr uint32_t value = 512u * U;
+};
 
 template <int U, int P>
-__device__ __forceinline__ void copy_chunk_warp(uint64_t s, uint64_t d, uint32_t len,
-                                                uint32_t lane)
+__device__ __forceinline__ void copy_pass(uint64_t s, uint64_t d, uint32_t len, uint32_t k,
+                                          uint32_t lane)
 {
-    if (len == 0)
-        return;
     if (((s ^ d) & 15u) == 0) {
-        if (s & 15u) {  // 8-byte head up to the 16-byte boundary
-            if (lane == 0)
-                st8<P>(reinterpret_cast<unsigned char *>(d),
-                       ld8(reinterpret_cast<const unsigned char *>(s)));
-            s += 8;
-            d += 8;
-            len -= 8;
-        }
-        const uint32_t n16 = len >> 4;
-        if ((len & 15u) && lane == 1) {  // 8-byte tail
-            const uint64_t o = (uint64_t)n16 << 4;
-            st8<P>(reinterpret_cast<unsigned char *>(d + o),
-                   ld8(reinterpret_cast<const unsigned char *>(s + o)));
-        }
-        const unsigned char *S = reinterpret_cast<const unsigned char *>(s);
-        unsigned char *D = reinterpret_cast<unsigned char *>(d);
-        for (uint32_t i0 = 0; i0 < n16; i0 += 32u * U) {
-            uint4 r[U];
-#pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const uint32_t idx = i0 + 32u * j + lane;
-                if (idx < n16)
-                    r[j] = ld16(S + ((uint64_t)idx << 4));
+        const uint32_t head = (s & 15u) ? 8u : 0u;  // len >= 8 whenever head != 0
+        const uint64_t bs = s + head, bd = d + head;
+        const uint32_t blen = len - head;
+        const uint32_t n16 = blen >> 4;
+        // the edge words of pass 0: lane 0 the head, lane 1 the tail
+        bool edge = false;
+        uint64_t es = 0, ed = 0;
+        if (k == 0) {
+            if (lane == 0 && head) {
+                edge = true;
+                es = s;
+                ed = d;
+            } else if (lane == 1 && (blen & 15u)) {
+                edge = true;
+                es = bs + ((uint64_t)n16 << 4);
+                ed = bd + ((uint64_t)n16 << 4);
             }
+        }
+        uint2 e = {0, 0};
+        if (edge)
+            e = ld8(reinterpret_cast<const unsigned char *>(es));
+        const unsigned char *S = reinterpret_cast<const unsigned char *>(bs);
+        unsigned char *D = reinterpret_cast<unsigned char *>(bd);
+        const uint32_t i0 = k * 32u * U;
+        uint4 r[U];
 #pragma unroll
-            for (int j = 0; j < U; ++j) {
-                const uint32_t idx = i0 + 32u * j + lane;
-                if (idx < n16)
-                    st16<P>(D + ((uint64_t)idx << 4), r[j]);
-            }
+        for (int j = 0; j < U; ++j) {
+            const uint32_t idx = i0 + 32u * j + lane;
+            if (idx < n16)
+                r[j] = ld16(S + ((uint64_t)idx << 4));
+        }
+        if (edge)
+            st8<P>(reinterpret_cast<unsigned char *>(ed), e);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const uint32_t idx = i0 + 32u * j + lane;
+            if (idx < n16)
+                st16<P>(D + ((uint64_t)idx << 4), r[j]);
         }
     } else {  // source and destination phases differ: 8-byte words throughout
         const uint32_t n8 = len >> 3;
         const unsigned char *S = reinterpret_cast<const unsigned char *>(s);
         unsigned char *D = reinterpret_cast<unsigned char *>(d);
-        for (uint32_t i0 = 0; i0 < n8; i0 += 64u * U) {
-            uint2 r[2 * U];
+        const uint32_t i0 = k * 64u * U;
+        uint2 r[2 * U];
 #pragma unroll
-            for (int j = 0; j < 2 * U; ++j) {
-                const uint32_t idx = i0 + 32u * j + lane;
-                if (idx < n8)
-                    r[j] = ld8(S + ((uint64_t)idx << 3));
-            }
+        for (int j = 0; j < 2 * U; ++j) {
+            const uint32_t idx = i0 + 32u * j + lane;
+            if (idx < n8)
+                r[j] = ld8(S + ((uint64_t)idx << 3));
+        }
 #pragma unroll
-            for (int j = 0; j < 2 * U; ++j) {
-                const uint32_t idx = i0 + 32u * j + lane;
-                if (idx < n8)
-                    st8<P>(D + ((uint64_t)idx << 3), r[j]);
-            }
+        for (int j = 0; j < 2 * U; ++j) {
+            const uint32_t idx = i0 + 32u * j + lane;
+            if (idx < n8)
+                st8<P>(D + ((uint64_t)idx << 3), r[j]);
         }
     }
+}
+
+// A whole chunk by one warp, pass after pass.
+template <int U, int P>
+__device__ __forceinline__ void copy_chunk_warp(uint64_t s, uint64_t d, uint32_t len,
+                                                uint32_t lane)
+{
+    for (uint32_t k = 0; k * PassBytes<U>::value < len; ++k)
+        copy_pass<U, P>(s, d, len, k, lane);
 }
 
 // A chunk record held in one lane's registers.
@@ -179,25 +205,39 @@ __device__ __forceinline__ Rec shfl_rec(const Rec &r, int src_lane)
 
 // ---- LDG variant -----------------------------------------------------------
 
+// Work units are warp passes in pass-major order: unit u is pass
+// u / n_chunks of chunk u % n_chunks, for `passes` passes per chunk (enough for
+// the batch's longest chunk). Unit u goes to warp u mod (warps in the grid).
+// Whatever the mix of chunk lengths, no warp ends with more than one pass more
+// than another, and for a batch of chunks that fit one pass every unit is a
+// whole chunk. A warp reads the records of its next 32 units with one load
+// per lane and hands them around with shuffles.
 template <int U, int P>
 __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
-                                                            uint32_t n_chunks)
+                                                            uint32_t n_chunks, uint32_t passes)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t wpb = blockDim.x >> 5;
     const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
-    // Chunks of this warp: gwarp + k * nwarps. Each pass takes 32 of them; lane l
-    // loads the record of the l-th.
-    for (uint64_t base = gwarp; base < n_chunks; base += 32u * nwarps) {
+    const uint64_t n_units = (uint64_t)n_chunks * passes;
+    for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
         const uint64_t mine = base + (uint64_t)lane * nwarps;
         Rec r = {0, 0, 0};
-        if (mine < n_chunks)
-            r = load_rec(tab, mine);
-        const int cnt = __popc(__ballot_sync(kFull, mine < n_chunks));
-        for (int k = 0; k < cnt; ++k) {
-            const Rec c = shfl_rec(r, k);
-            copy_chunk_warp<U, P>(c.s, c.d, c.l, lane);
+        uint32_t k = 0;
+        if (mine < n_units) {
+            const uint64_t pass = mine / n_chunks;
+            k = (uint32_t)pass;
+            r = load_rec(tab, mine - pass * n_chunks);
+            if ((uint64_t)k * PassBytes<U>::value >= r.l)
+                r.l = 0;  // this chunk has no pass k
+        }
+        const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
+        for (int j = 0; j < cnt; ++j) {
+            const Rec c = shfl_rec(r, j);
+            const uint32_t kk = __shfl_sync(kFull, k, j);
+            if (c.l)
+                copy_pass<U, P>(c.s, c.d, c.l, kk, lane);
         }
     }
 }
@@ -435,20 +475,21 @@ __global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns)
 }
 
 template <int U, int P>
-cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, cudaStream_t s)
+cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
+                       cudaStream_t s)
 {
-    kvx_copy_ldg_kernel<U, P><<<ctas, threads, 0, s>>>(t, n);
+    kvx_copy_ldg_kernel<U, P><<<ctas, threads, 0, s>>>(t, n, passes);
     return cudaGetLastError();
 }
 
 template <int U>
 cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint32_t n,
-                         cudaStream_t s)
+                         uint32_t passes, cudaStream_t s)
 {
     switch (p) {
-    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, s);
-    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, s);
-    default: return launch_ldg<U, 0>(ctas, threads, t, n, s);
+    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, s);
+    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, s);
+    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, s);
     }
 }
 
@@ -468,24 +509,33 @@ cudaError_t launch_bulk(int ctas, const kvx_chunk *t, uint32_t n, cudaStream_t s
 
 size_t bulk_smem_bytes(int stages) { return (size_t)stages * KVX_CHUNK_BYTES; }
 
-int work_ctas(const Launch &l, uint32_t n_chunks)
+uint32_t ldg_passes(const Launch &l, uint32_t max_chunk_len)
+{
+    const uint32_t unit = 512u * (uint32_t)l.unroll;
+    const uint32_t p = (max_chunk_len + unit - 1) / unit;
+    return p ? p : 1u;
+}
+
+int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
 {
     uint64_t need;
-    if (l.variant == KVX_VARIANT_BULK)
+    if (l.variant == KVX_VARIANT_BULK) {
         need = n_chunks;
-    else
-        need = (n_chunks + (uint64_t)(l.threads / 32) - 1) / (uint64_t)(l.threads / 32);
+    } else {
+        const uint64_t units = (uint64_t)n_chunks * ldg_passes(l, max_chunk_len);
+        need = (units + (uint64_t)(l.threads / 32) - 1) / (uint64_t)(l.threads / 32);
+    }
     if (need < 1)
         need = 1;
     return (int)((uint64_t)l.ctas < need ? (uint64_t)l.ctas : need);
 }
 
 cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
-                        cudaStream_t stream)
+                        uint32_t max_chunk_len, cudaStream_t stream)
 {
     if (n_chunks == 0)
         return cudaSuccess;
-    const int ctas = work_ctas(l, n_chunks);
+    const int ctas = work_ctas(l, n_chunks, max_chunk_len);
     if (l.variant == KVX_VARIANT_BULK) {
         switch (l.stages) {
         case 2: return launch_bulk<2>(ctas, table, n_chunks, stream);
@@ -493,10 +543,11 @@ cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chun
         default: return launch_bulk<3>(ctas, table, n_chunks, stream);
         }
     }
+    const uint32_t passes = ldg_passes(l, max_chunk_len);
     switch (l.unroll) {
-    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
-    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
-    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, table, n_chunks, stream);
+    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
+    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
+    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
     }
 }
 

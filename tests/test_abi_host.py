@@ -186,6 +186,18 @@ def test_capacity_limit():
     assert kvx.kvx_validate([1 << 20], [1 << 40], z, None, kvx.KVX_D2D, 0) == kvx.KVX_OK
 
 
+def test_huge_size_without_address_wrap_is_a_capacity_error():
+    # a size within 16 KiB of 2^64 whose address does not wrap
+    z = np.array([(1 << 64) - 16384 + 8], np.uint64)
+    assert kvx.kvx_validate([8], [16], z, None, kvx.KVX_D2D, 0) == kvx.KVX_ERR_CAPACITY
+    z = np.array([4096, 1 << 41], np.uint64)
+    assert kvx.kvx_validate([1 << 20, 1 << 21], [1 << 30, 1 << 31], z, None, kvx.KVX_D2D, 0) == \
+        kvx.KVX_ERR_CAPACITY
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_plan_chunks([8], [16], [(1 << 64) - 16384 + 8])
+    assert e.value.status == kvx.KVX_ERR_CAPACITY
+
+
 def test_copy_batch_rejects_before_any_cuda_call():
     s, d, z = _ok_batch()
     z[1] = 12
