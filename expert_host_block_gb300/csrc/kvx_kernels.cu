@@ -23,7 +23,8 @@
 //
 // Unaligned pieces: addresses and sizes are multiples of 8. When src and dst
 // have the same phase mod 16, a chunk is an 8-byte head, a 16-byte-word body
-// and an 8-byte tail; otherwise the whole chunk moves as 8-byte words.
+// and an 8-byte tail; otherwise aligned 16-byte source words are re-paired
+// across neighbouring lanes into aligned 16-byte destination words.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -87,11 +88,11 @@ __device__ __forceinline__ void st8(unsigned char *p, uint2 v)
 
 // ---- one warp pass over part of a chunk --------------------------------------
 //
-// A pass moves up to 512 * U bytes of one chunk: U 16-byte words per lane
-// (or 2U 8-byte words when source and destination differ in phase mod 16).
+// A pass moves up to 512 * U bytes of one chunk: U 16-byte words per lane.
 // Pass k of a chunk covers body words [k * 32U, (k + 1) * 32U); pass 0 also
-// moves the 8-byte head and tail. All loads of a pass are issued before any
-// of its stores, so a lane has U (or 2U, plus an edge word) loads in flight.
+// moves the 8-byte head (and, for matching phases, the tail). All loads of a
+// pass are issued before any of its stores, so a lane has U loads (plus at
+// most one edge word) in flight.
 
 template <int U>
 struct PassBytes {
@@ -142,23 +143,68 @@ __device__ __forceinline__ void copy_pass(uint64_t s, uint64_t d, uint32_t len, 
             if (idx < n16)
                 st16<P>(D + ((uint64_t)idx << 4), r[j]);
         }
-    } else {  // source and destination phases differ: 8-byte words throughout
-        const uint32_t n8 = len >> 3;
-        const unsigned char *S = reinterpret_cast<const unsigned char *>(s);
-        unsigned char *D = reinterpret_cast<unsigned char *>(d);
-        const uint32_t i0 = k * 64u * U;
-        uint2 r[2 * U];
-#pragma unroll
-        for (int j = 0; j < 2 * U; ++j) {
-            const uint32_t idx = i0 + 32u * j + lane;
-            if (idx < n8)
-                r[j] = ld8(S + ((uint64_t)idx << 3));
+    } else {
+        // Source and destination differ in phase mod 16 (one of them is 8 mod
+        // 16). If the source is the 16-aligned one, its first 8 bytes go out as
+        // a head word; after that the source is 8 mod 16 and the destination is
+        // 16-aligned. Destination word j is then the high half of the aligned
+        // source word V[j] and the low half of V[j + 1], where V[0] starts 8
+        // bytes before the (remaining) source range. Each V[j] read lies in a
+        // 16-byte block that holds source bytes, so no load leaves the pages of
+        // the source range; its out-of-range half is never stored.
+        bool edge = false;
+        uint2 e = {0, 0};
+        const uint64_t hd = d;
+        if ((s & 15u) == 0) {
+            if (k == 0 && lane == 0) {
+                edge = true;
+                e = ld8(reinterpret_cast<const unsigned char *>(s));
+            }
+            s += 8;
+            d += 8;
+            len -= 8;
         }
+        const unsigned char *V = reinterpret_cast<const unsigned char *>(s - 8);
+        unsigned char *D = reinterpret_cast<unsigned char *>(d);
+        const uint32_t n16 = len >> 4;
+        const bool tail = (len & 15u) != 0;
+        const uint32_t nv = (n16 || tail) ? n16 + 1 : 0;  // source words V[0 .. nv)
+        const uint32_t i0 = k * 32u * U;
+        uint4 r[U];
 #pragma unroll
-        for (int j = 0; j < 2 * U; ++j) {
+        for (int j = 0; j < U; ++j) {
             const uint32_t idx = i0 + 32u * j + lane;
-            if (idx < n8)
-                st8<P>(D + ((uint64_t)idx << 3), r[j]);
+            if (idx < nv)
+                r[j] = ld16(V + ((uint64_t)idx << 4));
+        }
+        uint2 x = {0, 0};  // lane 31: the low half of the word after this pass
+        const uint32_t ix = i0 + 32u * U;
+        if (lane == 31 && ix < nv) {
+            const uint4 t = ld16(V + ((uint64_t)ix << 4));
+            x = make_uint2(t.x, t.y);
+        }
+        if (edge)
+            st8<P>(reinterpret_cast<unsigned char *>(hd), e);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            uint32_t nx = __shfl_down_sync(kFull, r[j].x, 1);
+            uint32_t ny = __shfl_down_sync(kFull, r[j].y, 1);
+            if (j + 1 < U) {
+                const uint32_t fx = __shfl_sync(kFull, r[j + 1 < U ? j + 1 : j].x, 0);
+                const uint32_t fy = __shfl_sync(kFull, r[j + 1 < U ? j + 1 : j].y, 0);
+                if (lane == 31) {
+                    nx = fx;
+                    ny = fy;
+                }
+            } else if (lane == 31) {
+                nx = x.x;
+                ny = x.y;
+            }
+            const uint32_t idx = i0 + 32u * j + lane;
+            if (idx < n16)
+                st16<P>(D + ((uint64_t)idx << 4), make_uint4(r[j].z, r[j].w, nx, ny));
+            else if (idx == n16 && tail)
+                st8<P>(D + ((uint64_t)idx << 4), make_uint2(r[j].z, r[j].w));
         }
     }
 }
