@@ -38,7 +38,8 @@ def sources():
 
 
 def _inputs():
-    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    return (sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h")) +
+            [os.path.join(CSRC, "kvx.map")])
 
 
 def is_stale() -> bool:
@@ -74,7 +75,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("libkvx.so build failed:\n" + msg)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    link = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
+    link = [cc] + ARCH + ["-shared", "-cudart", "static", "-Xlinker",
+                          "--version-script=" + os.path.join(CSRC, "kvx.map"), "-o", tmp] + objs
     if verbose:
         print(" ".join(link))
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)

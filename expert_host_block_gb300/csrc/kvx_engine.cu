@@ -289,18 +289,59 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
     return m;
 }
 
+// Validation level 0 and packing in one pass over the descriptors, writing
+// at most `cap` records. Returns false (having written garbage) when any
+// descriptor fails a level-0 check or the records do not fit; the caller then
+// takes the exact two-pass path, which reports the first failing descriptor.
+bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+               kvx_chunk *out, size_t cap, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
+{
+    constexpr uint64_t kHuge = 1ull << 40;
+    uint64_t bad = 0, bytes = 0, longest = 0;
+    size_t m = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const uint64_t z = sizes[i], s = src[i], d = dst[i];
+        const uint64_t live = z ? ~0ull : 0ull;
+        bad |= live & (((s | d | z) & 7u) |
+                       ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d) | (z > kHuge)) << 3));
+        bytes += z;
+        longest = z > longest ? z : longest;
+        if (z <= KVX_CHUNK_BYTES) {
+            if (z) {
+                if (m >= cap)
+                    return false;
+                out[m++] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
+            }
+        } else {
+            if (bad || m + chunks_of(z) > cap)
+                return false;
+            for (uint64_t o = 0; o < z; o += KVX_CHUNK_BYTES)
+                out[m++] = kvx_chunk{s + o, d + o, (uint32_t)std::min<uint64_t>(KVX_CHUNK_BYTES, z - o),
+                                     (uint32_t)i, 0};
+        }
+    }
+    if (bad || m > KVX_MAX_CHUNKS)
+        return false;
+    *n_chunks = m;
+    *payload = bytes;
+    *max_chunk = (uint32_t)std::min<uint64_t>(longest, KVX_CHUNK_BYTES);
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // launch table
 // ---------------------------------------------------------------------------
-// Rows by direction and mean chunk size, from the calibration sweep on a
+// Rows by direction and mean chunk size, from the calibration sweeps on a
 // GB300 (NVLink-C2C host link). The host-link rows target bytes in flight
 // rather than threads (FreeToken issue #751, §Measured impact and §Proposal:
 // the optimum follows bytes in flight): one direction alone saturates the
-// link at about 512 KiB in flight (8 CTAs x 512 threads x 8 x 16 B), and H2D
-// and D2H running together need about 1.5 MiB per direction (24 CTAs). The
-// LDG variant reached the link peak in every measured size class with fewer
-// CTAs than the bulk ring, so every row picks it. D2D fills the GPU: one
-// 512-thread CTA per SM (107 registers a thread leave room for one).
+// link from about 512 KiB in flight (8 CTAs x 512 threads x 8 x 16 B) up to
+// the whole GPU, while H2D and D2H running together peak at about 2 MiB in
+// flight per direction (64 CTAs x 256 threads) and lose throughput beyond it,
+// as the pages saw PCIe collapse past its optimum. The LDG variant reached the
+// link peak in every measured size class with fewer CTAs than the bulk ring,
+// so every row picks it. D2D fills the GPU: one 512-thread CTA per SM (about
+// 120 registers a thread leave room for one).
 struct TableRow {
     int dir;
     uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
@@ -308,8 +349,8 @@ struct TableRow {
 };
 
 const TableRow kTable[] = {
-    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 24, 512, 8, 3, 0}},
-    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 24, 512, 8, 3, 0}},
+    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
+    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0}},
 };
 
@@ -466,6 +507,50 @@ struct StatusWords {
 StatusWords g_status_words[kMaxDevices];
 constexpr unsigned kStatusWords = 1024;
 
+// The common case of kvx_copy_batch_ex in one pass over the descriptors:
+// level-0 validation fused with packing into the staging slot. Sets *done and
+// returns the call's status once it has enqueued (or failed to enqueue) the
+// copy; leaves *done false, with nothing enqueued, whenever anything is off
+// (capture, a bad descriptor, a full slot), so that the exact path decides.
+kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                           int dir, const kvx_launch *want, cudaStream_t stream, bool *done)
+{
+    *done = false;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return KVX_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return KVX_OK;
+    }
+    Slot *s = nullptr;
+    if (ring_acquire(dev, n, &s) != KVX_OK)
+        return KVX_OK;
+    uint64_t chunks = 0, payload = 0;
+    uint32_t max_chunk = 0;
+    Launch l;
+    if (!pack_fast(src, dst, sizes, n, s->host, s->cap, &chunks, &payload, &max_chunk) || chunks == 0 ||
+        resolve(dir, payload / chunks, want, &l) != KVX_OK) {
+        ring_release(dev, s, stream, false);
+        return KVX_OK;
+    }
+    *done = true;
+    cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
+                                    cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        ring_release(dev, s, stream, false);
+        return cuda_fail(e, "cudaMemcpyAsync(chunk table)");
+    }
+    e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, max_chunk, stream);
+    ring_release(dev, s, stream, true);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy kernel launch");
+    return KVX_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -565,6 +650,12 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
+    if (n && src && dst && sizes && dir >= KVX_H2D && dir <= KVX_D2D && validate_level() == 0) {
+        bool done = false;
+        st = copy_batch_fast(src, dst, sizes, n, dir, want, stream, &done);
+        if (done)
+            return st;
+    }
     uint64_t chunks = 0, payload = 0;
     uint32_t max_chunk = 0;
     st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);

@@ -377,3 +377,80 @@ def test_bounded_wait_times_out_and_context_survives():
         _one(p, w.batches[0])
     finally:
         p.close()
+
+
+# ---- the fused validate+pack path of kvx_copy_batch (validation level 0) ---------
+
+@pytest.fixture
+def level0():
+    kvx.kvx_set_validate_level(0)
+    yield
+    kvx.kvx_set_validate_level(1)
+
+
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+@pytest.mark.parametrize("odd", [False, True])
+def test_level0_sweep_cells(level0, direction, odd):
+    w = W.sweep_cell(24, 2000, direction, odd_tails=odd)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0])
+    finally:
+        p.close()
+
+
+def test_level0_kv_burst_and_moe(level0):
+    w = W.kv_burst(n_sets=2, n_per_dir=8192, pool_bytes=256 * W.MIB)
+    p = Pools(w.pools)
+    try:
+        want = p.expected([b for pair in w.batches for b in pair])
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        for h2d, d2h in w.batches:
+            run_batch(p, h2d, stream=s1)
+            run_batch(p, d2h, stream=s2)
+        kvx.kvx_stream_check(s1)
+        kvx.kvx_stream_check(s2)
+        p.assert_equal(want)
+    finally:
+        p.close()
+    m = W.MoeGather(n_slots=200)
+    p = Pools(m.pools)
+    try:
+        calls = [m.next_call() for _ in range(2)]
+        want = p.expected(calls)
+        for b in calls:
+            run_batch(p, b)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+def test_level0_batch_larger_than_a_staging_slot(level0):
+    """70,000 one-chunk descriptors: more than a fresh slot holds, so the exact path grows it."""
+    n = 70_000
+    p = _pools_small("device", "device", body=2 * W.MIB)
+    try:
+        g = np.random.default_rng(5)
+        dst = g.permutation(2 * W.MIB // 16)[:n].astype(np.uint64) * np.uint64(16)
+        src = g.integers(0, 2 * W.MIB // 8, n).astype(np.uint64) * np.uint64(8)
+        _one(p, _batch(src, dst, np.full(n, 8), "d2d"))
+    finally:
+        p.close()
+
+
+def test_level0_errors_still_reported(level0):
+    p = _pools_small()
+    try:
+        want = p.expected([])
+        hs, dd = p.base("src"), p.base("dst")
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_copy_batch([hs, hs + 8192], [dd, dd + 8192], [4096, 4100], None, "h2d", 0, None)
+        assert e.value.status == kvx.KVX_ERR_ALIGN
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_copy_batch([hs, 0], [dd, dd + 8192], [4096, 4096], None, "h2d", 0, None)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
