@@ -289,42 +289,30 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
     return m;
 }
 
-// Validation level 0 and packing in one pass over the descriptors, writing
-// at most `cap` records. Returns false (having written garbage) when any
-// descriptor fails a level-0 check or the records do not fit; the caller then
-// takes the exact two-pass path, which reports the first failing descriptor.
+// Validation level 0 and packing in one pass, for the common batch of many
+// descriptors that each fit one chunk: record i is descriptor i (a zero-size
+// descriptor becomes an empty record, which the kernels skip). Needs cap >= n.
+// Returns false (having written garbage) when a descriptor fails a level-0
+// check or is longer than one chunk; the caller then takes the exact two-pass
+// path, which also reports the first failing descriptor.
 bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
-               kvx_chunk *out, size_t cap, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
+               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
 {
-    constexpr uint64_t kHuge = 1ull << 40;
     uint64_t bad = 0, bytes = 0, longest = 0;
-    size_t m = 0;
     for (size_t i = 0; i < n; ++i) {
         const uint64_t z = sizes[i], s = src[i], d = dst[i];
         const uint64_t live = z ? ~0ull : 0ull;
-        bad |= live & (((s | d | z) & 7u) |
-                       ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d) | (z > kHuge)) << 3));
+        bad |= live & (((s | d | z) & 7u) | ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d)) << 3));
+        bad |= (uint64_t)(z > KVX_CHUNK_BYTES) << 4;
         bytes += z;
         longest = z > longest ? z : longest;
-        if (z <= KVX_CHUNK_BYTES) {
-            if (z) {
-                if (m >= cap)
-                    return false;
-                out[m++] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
-            }
-        } else {
-            if (bad || m + chunks_of(z) > cap)
-                return false;
-            for (uint64_t o = 0; o < z; o += KVX_CHUNK_BYTES)
-                out[m++] = kvx_chunk{s + o, d + o, (uint32_t)std::min<uint64_t>(KVX_CHUNK_BYTES, z - o),
-                                     (uint32_t)i, 0};
-        }
+        out[i] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
     }
-    if (bad || m > KVX_MAX_CHUNKS)
+    if (bad || n > KVX_MAX_CHUNKS)
         return false;
-    *n_chunks = m;
+    *n_chunks = n;
     *payload = bytes;
-    *max_chunk = (uint32_t)std::min<uint64_t>(longest, KVX_CHUNK_BYTES);
+    *max_chunk = (uint32_t)longest;
     return true;
 }
 
@@ -420,12 +408,13 @@ struct Slot {
     cudaEvent_t done = nullptr;
     bool recorded = false;
     bool busy = false;          // held by a caller between acquire and release
+    uint64_t stamp = 0;         // release order: larger = more recently packed
 };
 
 struct Ring {
     std::mutex mu;
     Slot slots[kRingSlots];
-    unsigned next = 0;
+    uint64_t clock = 0;
 };
 
 Ring g_rings[kMaxDevices];
@@ -437,12 +426,29 @@ kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
     Ring &r = g_rings[dev];
     Slot *s = nullptr;
     {
+        // Prefer the most recently packed slot whose copy has finished: its
+        // pinned pages are still in the CPU caches, so packing into it avoids
+        // fetching a cold slot's lines from memory. Otherwise take the least
+        // recently used free slot and wait for its copy below.
         std::lock_guard<std::mutex> g(r.mu);
-        for (int t = 0; t < kRingSlots && !s; ++t) {
-            Slot &c = r.slots[r.next++ % kRingSlots];
-            if (!c.busy)
-                s = &c;
+        Slot *warm = nullptr, *oldest = nullptr;
+        for (Slot &c : r.slots) {
+            if (c.busy)
+                continue;
+            if (!oldest || c.stamp < oldest->stamp)
+                oldest = &c;
+            if (c.cap < chunks || (warm && c.stamp <= warm->stamp))
+                continue;
+            if (c.recorded) {
+                if (cudaEventQuery(c.done) != cudaSuccess) {
+                    cudaGetLastError();  // cudaErrorNotReady is not sticky; clear it
+                    continue;
+                }
+                c.recorded = false;
+            }
+            warm = &c;
         }
+        s = warm ? warm : oldest;
         if (!s)
             return fail(KVX_ERR_CAPACITY, "all %d staging slots are held by concurrent callers", kRingSlots);
         s->busy = true;
@@ -495,6 +501,7 @@ void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
     if (record && cudaEventRecord(s->done, stream) == cudaSuccess)
         s->recorded = true;
     std::lock_guard<std::mutex> g(g_rings[dev].mu);
+    s->stamp = ++g_rings[dev].clock;
     s->busy = false;
 }
 
@@ -526,13 +533,15 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
         cudaGetLastError();
         return KVX_OK;
     }
+    if (n > KVX_MAX_CHUNKS)
+        return KVX_OK;
     Slot *s = nullptr;
     if (ring_acquire(dev, n, &s) != KVX_OK)
         return KVX_OK;
     uint64_t chunks = 0, payload = 0;
     uint32_t max_chunk = 0;
     Launch l;
-    if (!pack_fast(src, dst, sizes, n, s->host, s->cap, &chunks, &payload, &max_chunk) || chunks == 0 ||
+    if (!pack_fast(src, dst, sizes, n, s->host, &chunks, &payload, &max_chunk) || payload == 0 ||
         resolve(dir, payload / chunks, want, &l) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;

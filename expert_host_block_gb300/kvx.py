@@ -197,6 +197,45 @@ def kvx_copy_batch_ex(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, launch=N
                                      ctypes.byref(lp) if lp is not None else None, _stream(stream)))
 
 
+class Descriptors:
+    """Reusable descriptor arrays with their addresses taken once.
+
+    The vLLM offloading connector keeps its descriptor arrays as buffers it
+    allocates once and refills for every transfer (vLLM PR #42212 report,
+    §实现拆解 item 3). This is that pattern on the Python side: three uint64
+    arrays of a fixed capacity whose addresses are looked up at construction,
+    so a call only marshals integers. Fill ``src``, ``dst`` and ``sizes``
+    (directly, or with ``set``), then call ``copy_batch``.
+    """
+
+    def __init__(self, capacity: int):
+        self.capacity = int(capacity)
+        self.src = np.zeros(self.capacity, dtype=np.uint64)
+        self.dst = np.zeros(self.capacity, dtype=np.uint64)
+        self.sizes = np.zeros(self.capacity, dtype=np.uint64)
+        self.n = 0
+        self._ptrs = (self.src.ctypes.data, self.dst.ctypes.data, self.sizes.ctypes.data)
+        self._fn = _load().kvx_copy_batch
+
+    def set(self, src_addrs, dst_addrs, sizes) -> "Descriptors":
+        n = len(sizes)
+        if n > self.capacity:
+            raise ValueError(f"{n} descriptors exceed capacity {self.capacity}")
+        self.src[:n] = src_addrs
+        self.dst[:n] = dst_addrs
+        self.sizes[:n] = sizes
+        self.n = n
+        return self
+
+    def copy_batch(self, dir, cta_budget: int = 0, stream=None) -> None:
+        """kvx_copy_batch over the first ``n`` descriptors."""
+        ps, pd, pz = self._ptrs
+        st = self._fn(ps, pd, pz, self.n, DIRS[dir] if isinstance(dir, str) else dir, cta_budget,
+                      _stream(stream))
+        if st != KVX_OK:
+            raise KvxError(st, last_error())
+
+
 # ---- descriptor buffers ----------------------------------------------------
 
 def kvx_desc_buf_create(max_chunks: int) -> int:

@@ -126,8 +126,10 @@ typedef struct kvx_desc_buf kvx_desc_buf;
  * every direction). `cta_budget`: 0 = calibrated default, > 0 = at most that
  * many CTAs, < 0 = KVX_ERR_INVALID_ARG. Not allowed during stream capture
  * (KVX_ERR_CAPTURE): it writes a pinned staging slot on the host. The staging
- * ring has 8 slots per device; a call waits on the host only when the slot it
- * takes is still in use by a call eight calls back. */
+ * ring has 8 slots per device; a call takes the most recently used slot whose
+ * copy has finished, and waits on the host only when none has (then for the
+ * least recently used one). A slot allocates on first use and grows, once, for
+ * a batch bigger than it holds. */
 kvx_status kvx_copy_batch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                           const uint64_t *sizes, size_t n, int dir, int cta_budget,
                           void *stream);

@@ -256,3 +256,14 @@ def test_unknown_env_values_are_errors(var, val):
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
     assert out.stdout.startswith(f"{kvx.KVX_ERR_INVALID_ARG} "), out.stdout + out.stderr
     assert var in out.stdout
+
+
+def test_descriptors_helper_fill_and_capacity():
+    d = kvx.Descriptors(4).set([8, 16], [24, 32], [8, 8])
+    assert d.n == 2 and list(d.src[:2]) == [8, 16] and list(d.sizes[:2]) == [8, 8]
+    with pytest.raises(ValueError):
+        d.set([8] * 5, [16] * 5, [8] * 5)
+    d.sizes[1] = 12  # refilled in place: validation still applies
+    with pytest.raises(kvx.KvxError) as e:
+        d.copy_batch("h2d")
+    assert e.value.status == kvx.KVX_ERR_ALIGN
