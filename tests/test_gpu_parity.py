@@ -463,10 +463,8 @@ def test_descriptors_helper_parity(level0):
         want = p.expected([b for pair in w.batches for b in pair])
         dh, dd = kvx.Descriptors(4096), kvx.Descriptors(4096)
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-        for h2d, d2h in w.batches:  # refilled in place for every set
-            s1.synchronize()
+        for h2d, d2h in w.batches:  # refilled in place as soon as each call returns
             dh.set(*p.addrs(h2d)).copy_batch("h2d", 0, s1)
-            s2.synchronize()
             dd.set(*p.addrs(d2h)).copy_batch("d2h", 0, s2)
         kvx.kvx_stream_check(s1)
         kvx.kvx_stream_check(s2)
