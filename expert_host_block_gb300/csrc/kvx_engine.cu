@@ -582,6 +582,15 @@ struct kvx_desc_buf {
     kvx_launch selected{};
 };
 
+struct kvx_devlist {
+    int device = 0;
+    uint32_t max_n = 0;
+    kvx::DevListMeta *meta = nullptr;  // 256 bytes, then the offsets
+    uint64_t *offsets = nullptr;
+    cudaEvent_t last_use = nullptr;
+    bool use_recorded = false;
+};
+
 // ---------------------------------------------------------------------------
 // C ABI
 // ---------------------------------------------------------------------------
@@ -879,6 +888,82 @@ kvx_status kvx_desc_buf_destroy(kvx_desc_buf *b)
     return KVX_OK;
 }
 
+kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out)
+{
+    if (!out)
+        return fail(KVX_ERR_INVALID_ARG, "null output");
+    *out = nullptr;
+    if (max_n < 1 || max_n > (1u << 24))
+        return fail(KVX_ERR_CAPACITY, "max_n %u not in 1..2^24", max_n);
+    kvx_devlist *l = new (std::nothrow) kvx_devlist;
+    if (!l)
+        return fail(KVX_ERR_CAPACITY, "out of host memory");
+    l->max_n = max_n;
+    cudaError_t e = cudaGetDevice(&l->device);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&l->meta),
+                       256 + ((size_t)max_n + 1) * sizeof(uint64_t));
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&l->last_use, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (l->meta)
+            cudaFree(l->meta);
+        delete l;
+        return cuda_fail(e, "kvx_devlist_create");
+    }
+    l->offsets = reinterpret_cast<uint64_t *>(reinterpret_cast<char *>(l->meta) + 256);
+    *out = l;
+    return KVX_OK;
+}
+
+kvx_status kvx_devlist_destroy(kvx_devlist *l)
+{
+    if (!l)
+        return KVX_OK;
+    if (l->use_recorded)
+        cudaEventSynchronize(l->last_use);
+    cudaFree(l->meta);
+    cudaEventDestroy(l->last_use);
+    delete l;
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint64_t *dst,
+                                const uint64_t *sizes, const uint32_t *count, int dir,
+                                const kvx_launch *want, void *stream_)
+{
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!l)
+        return fail(KVX_ERR_INVALID_ARG, "null device list");
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    if (!src || !dst || !sizes || !count)
+        return fail(KVX_ERR_INVALID_ARG, "null device array");
+    if (((uintptr_t)src | (uintptr_t)dst | (uintptr_t)sizes) & 7u || (uintptr_t)count & 3u)
+        return fail(KVX_ERR_ALIGN, "device arrays must be 8-byte aligned (the count 4-byte aligned)");
+    if (dir < KVX_H2D || dir > KVX_D2D)
+        return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
+    Launch lc;
+    st = resolve(dir, KVX_CHUNK_BYTES, want, &lc);
+    if (st != KVX_OK)
+        return st;
+    if (lc.variant != KVX_VARIANT_LDG)
+        return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
+    bool cap = false;
+    st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
+    cudaError_t e = kvx::launch_devlist(lc, src, dst, sizes, count, l->max_n, l->meta, l->offsets, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device-list launch");
+    if (!cap) {
+        KVX_CUDA_TRY(cudaEventRecord(l->last_use, stream));
+        l->use_recorded = true;
+    }
+    return KVX_OK;
+}
+
 kvx_status kvx_stream_check(void *stream_)
 {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -903,7 +988,10 @@ kvx_status kvx_stream_check(void *stream_)
     if (bits & kvx::kDevErrTimeout)
         return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
     if (bits)
-        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x", bits);
+        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s", bits,
+                    (bits & kvx::kDevErrBadRecord) ? " chunk record longer than KVX_CHUNK_BYTES;" : "",
+                    (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
+                    (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
     return KVX_OK;
 }
 

@@ -15,6 +15,15 @@ namespace kvx {
 enum : unsigned {
     kDevErrTimeout = 1u,    // a bounded mbarrier wait gave up
     kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES
+    kDevErrCount = 4u,      // a device-side descriptor count above the list's capacity (clamped)
+    kDevErrBadDesc = 8u,    // a device-side descriptor failed validation (skipped)
+};
+
+// Result of the device-list plan kernel, read by the device-list copy kernel.
+struct DevListMeta {
+    uint64_t total;      // chunks of the valid descriptors
+    uint32_t n;          // descriptors taken (the count, clamped to the capacity)
+    uint32_t max_chunk;  // longest chunk, bytes
 };
 
 // Bounded-wait limit of the bulk kernel's mbarrier waits (ns of %globaltimer).
@@ -38,6 +47,13 @@ int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
 // the longest record's len (it sets the LDG kernel's passes per chunk).
 cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
                         uint32_t max_chunk_len, cudaStream_t stream);
+
+// Enqueue the plan and copy kernels over a device-resident descriptor list:
+// count and arrays in device memory, meta and offsets[max_n + 1] scratch.
+// l.ctas is used as is (the work is not known on the host).
+cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t *dst,
+                           const uint64_t *sizes, const uint32_t *count, uint32_t max_n,
+                           DevListMeta *meta, uint64_t *offsets, cudaStream_t stream);
 
 // Enqueue a 1-thread kernel that moves the status word into *host_word
 // (mapped pinned) and clears it.

@@ -497,6 +497,157 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     __syncwarp();
 }
 
+// ---- descriptors that live on the device -------------------------------------
+//
+// A producer kernel (a MoE router, a block manager on the GPU) writes the
+// descriptor arrays and their count in device memory; the host never sees
+// them, so the copy is two fixed-shape launches that can be captured in a
+// CUDA graph (FreeToken issue #751, §What we changed: the miss count is read
+// on the device, so the launch is fixed-shape and capturable). The plan
+// kernel validates the list and writes the exclusive scan of chunk counts;
+// the copy kernel maps each warp pass to (descriptor, chunk) by binary search
+// over that scan.
+
+// One CTA: clamp the count, validate, scan chunk counts into offsets[0..n].
+__global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
+    const uint64_t *__restrict__ src, const uint64_t *__restrict__ dst,
+    const uint64_t *__restrict__ sizes, const uint32_t *__restrict__ count, uint32_t max_n,
+    DevListMeta *__restrict__ meta, uint64_t *__restrict__ offsets)
+{
+    __shared__ uint64_t warp_sums[32];
+    __shared__ uint64_t s_carry;
+    __shared__ uint32_t s_max, s_bad;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
+    const uint32_t nwarps = blockDim.x >> 5;
+    uint32_t n = *count;
+    if (n > max_n) {
+        if (tid == 0)
+            atomicOr(&g_status, kDevErrCount);
+        n = max_n;
+    }
+    if (tid == 0) {
+        s_carry = 0;
+        s_max = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
+    for (uint32_t base = 0; base < n; base += blockDim.x) {
+        const uint32_t i = base + tid;
+        uint64_t c = 0;
+        if (i < n) {
+            const uint64_t z = sizes[i];
+            if (z) {
+                const uint64_t a = src[i], b = dst[i];
+                if (((a | b | z) & 7u) || !a || !b || a + z < a || b + z < b || z > (1ull << 40)) {
+                    atomicOr(&s_bad, 1u);  // skipped: contributes no chunks
+                } else {
+                    c = z / KVX_CHUNK_BYTES + (z % KVX_CHUNK_BYTES != 0);
+                    atomicMax(&s_max, (uint32_t)(z < KVX_CHUNK_BYTES ? z : KVX_CHUNK_BYTES));
+                }
+            }
+        }
+        uint64_t x = c;  // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= (uint32_t)o)
+                x += y;
+        }
+        if (lane == 31)
+            warp_sums[wid] = x;
+        __syncthreads();
+        if (wid == 0) {  // scan of the warp totals
+            uint64_t w = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(kFull, w, o);
+                if (lane >= (uint32_t)o)
+                    w += y;
+            }
+            if (lane < nwarps)
+                warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const uint64_t before = s_carry + (wid ? warp_sums[wid - 1] : 0);
+        if (i < n)
+            offsets[i] = before + x - c;
+        __syncthreads();
+        if (tid == 0)
+            s_carry += warp_sums[nwarps - 1];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        offsets[n] = s_carry;
+        meta->total = s_carry;
+        meta->n = n;
+        meta->max_chunk = s_max;
+        if (s_bad)
+            atomicOr(&g_status, kDevErrBadDesc);
+    }
+}
+
+constexpr uint32_t kSmemOffsets = 4096;  // scans of up to 4,095 descriptors are searched in shared memory
+
+template <int U, int P>
+__global__ void __launch_bounds__(512) kvx_copy_devlist_kernel(
+    const uint64_t *__restrict__ src, const uint64_t *__restrict__ dst,
+    const uint64_t *__restrict__ sizes, const DevListMeta *__restrict__ meta,
+    const uint64_t *__restrict__ offsets)
+{
+    __shared__ uint64_t s_off[kSmemOffsets];
+    const uint64_t total = meta->total;
+    const uint32_t n = meta->n;
+    if (total == 0)
+        return;
+    const bool in_smem = n + 1 <= kSmemOffsets;
+    if (in_smem) {
+        for (uint32_t i = threadIdx.x; i <= n; i += blockDim.x)
+            s_off[i] = offsets[i];
+        __syncthreads();
+    }
+    const uint32_t unit = PassBytes<U>::value;
+    const uint32_t passes = meta->max_chunk ? (meta->max_chunk + unit - 1) / unit : 1u;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t wpb = blockDim.x >> 5;
+    const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
+    const uint64_t n_units = total * passes;
+    for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
+        const uint64_t mine = base + (uint64_t)lane * nwarps;
+        Rec r = {0, 0, 0};
+        uint32_t k = 0;
+        if (mine < n_units) {
+            const uint64_t pass = mine / total;
+            const uint64_t c = mine - pass * total;
+            k = (uint32_t)pass;
+            // offsets[lo] <= c < offsets[hi], with offsets[0] = 0 and offsets[n] = total
+            uint32_t lo = 0, hi = n;
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) >> 1;
+                const uint64_t o = in_smem ? s_off[mid] : __ldg(offsets + mid);
+                if (o <= c)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const uint64_t j = c - (in_smem ? s_off[lo] : __ldg(offsets + lo));
+            const uint64_t z = sizes[lo], off = j * KVX_CHUNK_BYTES;
+            r.s = src[lo] + off;
+            r.d = dst[lo] + off;
+            r.l = (uint32_t)(z - off < KVX_CHUNK_BYTES ? z - off : KVX_CHUNK_BYTES);
+            if ((uint64_t)k * unit >= r.l)
+                r.l = 0;
+        }
+        const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
+        for (int jj = 0; jj < cnt; ++jj) {
+            const Rec cc = shfl_rec(r, jj);
+            const uint32_t kk = __shfl_sync(kFull, k, jj);
+            if (cc.l)
+                copy_pass<U, P>(cc.s, cc.d, cc.l, kk, lane);
+        }
+    }
+}
+
 // ---- status word and the bounded-wait self-test ---------------------------
 
 __global__ void kvx_status_fetch_kernel(unsigned *host_word)
@@ -551,6 +702,19 @@ cudaError_t launch_bulk(int ctas, const kvx_chunk *t, uint32_t n, cudaStream_t s
     return cudaGetLastError();
 }
 
+template <int U>
+cudaError_t launch_devlist_p(int p, int ctas, int threads, const uint64_t *src, const uint64_t *dst,
+                            const uint64_t *sizes, const DevListMeta *meta, const uint64_t *offsets,
+                            cudaStream_t s)
+{
+    switch (p) {
+    case 1: kvx_copy_devlist_kernel<U, 1><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
+    case 2: kvx_copy_devlist_kernel<U, 2><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
+    default: kvx_copy_devlist_kernel<U, 0><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t bulk_smem_bytes(int stages) { return (size_t)stages * KVX_CHUNK_BYTES; }
@@ -594,6 +758,21 @@ cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chun
     case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
     case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
     default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
+    }
+}
+
+cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t *dst,
+                           const uint64_t *sizes, const uint32_t *count, uint32_t max_n,
+                           DevListMeta *meta, uint64_t *offsets, cudaStream_t stream)
+{
+    kvx_devlist_plan_kernel<<<1, 1024, 0, stream>>>(src, dst, sizes, count, max_n, meta, offsets);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    switch (l.unroll) {
+    case 2: return launch_devlist_p<2>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
+    case 4: return launch_devlist_p<4>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
+    default: return launch_devlist_p<8>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
     }
 }
 

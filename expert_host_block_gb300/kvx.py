@@ -53,6 +53,7 @@ EXPORTS = (
     "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version",
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
     "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
+    "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
@@ -112,6 +113,9 @@ def _load():
         "kvx_copy_contiguous": ([_u64, _u64, _u64, _int, _vp], _int),
         "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
         "kvx_copy_batch_noalloc": ([_vp, _vp, _vp, _sz, _int, _int, _vp], _int),
+        "kvx_devlist_create": ([ctypes.c_uint32, ctypes.POINTER(_vp)], _int),
+        "kvx_devlist_destroy": ([_vp], _int),
+        "kvx_copy_device_list": ([_vp, _u64, _u64, _u64, _u64, _int, ctypes.POINTER(kvx_launch), _vp], _int),
         "kvx_standin_gemv_bf16": ([_u64, _u64, _u64, _u64, ctypes.c_uint32, _int, _vp], _int),
     }
     for name, (args, res) in sig.items():
@@ -300,6 +304,48 @@ class DescBuf:
 
     def __exit__(self, *exc):
         self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- descriptor lists that live on the device --------------------------------
+
+def kvx_devlist_create(max_n: int) -> int:
+    h = _vp()
+    _check(_load().kvx_devlist_create(int(max_n), ctypes.byref(h)))
+    return h.value
+
+
+def kvx_devlist_destroy(handle: int) -> None:
+    _check(_load().kvx_devlist_destroy(handle))
+
+
+def kvx_copy_device_list(handle: int, d_src: int, d_dst: int, d_sizes: int, d_count: int, dir,
+                         launch=None, stream=None) -> None:
+    """Copy the list whose arrays and count are in device memory (device addresses)."""
+    lp = _launch(launch)
+    _check(_load().kvx_copy_device_list(handle, int(d_src), int(d_dst), int(d_sizes), int(d_count), _dir(dir),
+                                        ctypes.byref(lp) if lp is not None else None, _stream(stream)))
+
+
+class DeviceList:
+    """A kvx_devlist owned by a Python object."""
+
+    def __init__(self, max_n: int):
+        self.handle = kvx_devlist_create(max_n)
+        self.max_n = int(max_n)
+
+    def copy(self, d_src: int, d_dst: int, d_sizes: int, d_count: int, dir, launch=None, stream=None):
+        kvx_copy_device_list(self.handle, d_src, d_dst, d_sizes, d_count, dir, launch, stream)
+
+    def close(self):
+        if self.handle:
+            kvx_devlist_destroy(self.handle)
+            self.handle = 0
 
     def __del__(self):
         try:

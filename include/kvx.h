@@ -170,6 +170,43 @@ kvx_status kvx_desc_buf_info(const kvx_desc_buf *buf, size_t *n_chunks,
 /* Wait for the buffer's last upload and last copy, then free it. */
 kvx_status kvx_desc_buf_destroy(kvx_desc_buf *buf);
 
+/* ---- descriptor lists that live on the device ---------------------------- */
+
+/* A producer on the GPU (a MoE router choosing missed experts, a block manager
+ * choosing KV pages) can write the descriptor arrays and their count in device
+ * memory. Then the host knows neither, and the copy must be a fixed-shape
+ * launch that reads the count on the device, so that it can be captured in a
+ * CUDA graph and replayed with new contents (FreeToken issue #751, §What we
+ * changed: "the miss count is read on the device, so the launch is
+ * fixed-shape and CUDA-graph capturable").
+ *
+ * A kvx_devlist holds the device scratch of such copies for lists of up to
+ * max_n descriptors: 16 bytes of plan results and (max_n + 1) 64-bit chunk
+ * offsets. Create it outside capture (it allocates device memory). */
+typedef struct kvx_devlist kvx_devlist;
+
+kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out); /* 1 <= max_n <= 2^24 */
+kvx_status kvx_devlist_destroy(kvx_devlist *list);                /* waits for its last copy */
+
+/* Enqueue the copy of the device-resident list: d_src, d_dst and d_sizes are
+ * device arrays of at least max_n uint64 each (same meaning and rules as the
+ * host arrays of kvx_copy_batch), d_count a device uint32 holding n. Two
+ * launches on `stream`: a one-CTA plan kernel (validates, scans chunk
+ * counts) and the LDG copy kernel with launch->cta_budget CTAs (the grid is
+ * not clamped to the work, which the host does not know). No host work, no
+ * allocation, no synchronisation: allowed inside stream capture; replaying
+ * the graph copies whatever the arrays and count hold at replay time.
+ * Host-side errors (null or misaligned arrays, bad dir or launch, a BULK
+ * variant) return without enqueuing. Device-side problems are reported by
+ * kvx_stream_check as KVX_ERR_DEVICE_FAULT: a count above max_n (only max_n
+ * descriptors are copied) or a descriptor that fails validation (it is
+ * skipped; the others are copied). Overlapping destinations are not
+ * detected. The list's scratch is reused by every call: calls with the same
+ * list on different streams must not overlap. */
+kvx_status kvx_copy_device_list(kvx_devlist *list, const uint64_t *d_src, const uint64_t *d_dst,
+                                const uint64_t *d_sizes, const uint32_t *d_count, int dir,
+                                const kvx_launch *launch, void *stream);
+
 /* ---- host-only helpers (no CUDA call, no GPU needed) -------------------- */
 
 /* Validate a batch at `level` (0: arrays, dir, alignment, overflow, capacity;
