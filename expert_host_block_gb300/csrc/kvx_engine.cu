@@ -562,6 +562,11 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
 
 }  // namespace
 
+kvx_status kvx::set_error(kvx_status status, const char *message)
+{
+    return fail(status, "%s", message);
+}
+
 // ---------------------------------------------------------------------------
 // descriptor buffers
 // ---------------------------------------------------------------------------

@@ -59,6 +59,9 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
 // (mapped pinned) and clears it.
 cudaError_t launch_status_fetch(unsigned *host_word, cudaStream_t stream);
 
+// Set the calling thread's kvx_last_error() message and return `status`.
+kvx_status set_error(kvx_status status, const char *message);
+
 // Enqueue the bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
 

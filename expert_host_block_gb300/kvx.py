@@ -54,6 +54,8 @@ EXPORTS = (
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
     "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
+    "kvx_transfer_create", "kvx_transfer_start", "kvx_transfer_poll", "kvx_transfer_progress",
+    "kvx_transfer_destroy",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
@@ -114,6 +116,11 @@ def _load():
         "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
         "kvx_copy_batch_noalloc": ([_vp, _vp, _vp, _sz, _int, _int, _vp], _int),
         "kvx_devlist_create": ([ctypes.c_uint32, ctypes.POINTER(_vp)], _int),
+        "kvx_transfer_create": ([ctypes.POINTER(_vp)], _int),
+        "kvx_transfer_start": ([_vp, _vp, _vp, _vp, _sz, _int, _sz, ctypes.POINTER(kvx_launch), _vp], _int),
+        "kvx_transfer_poll": ([_vp, ctypes.POINTER(_int)], _int),
+        "kvx_transfer_progress": ([_vp, ctypes.POINTER(_sz), ctypes.POINTER(_sz)], _int),
+        "kvx_transfer_destroy": ([_vp], _int),
         "kvx_devlist_destroy": ([_vp], _int),
         "kvx_copy_device_list": ([_vp, _u64, _u64, _u64, _u64, _int, ctypes.POINTER(kvx_launch), _vp], _int),
         "kvx_standin_gemv_bf16": ([_u64, _u64, _u64, _u64, ctypes.c_uint32, _int, _vp], _int),
@@ -345,6 +352,46 @@ class DeviceList:
     def close(self):
         if self.handle:
             kvx_devlist_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---- tail-bounded submission ---------------------------------------------------
+
+class Transfer:
+    """A kvx_transfer: a batch submitted in pieces, each after the previous one completed."""
+
+    def __init__(self):
+        h = _vp()
+        _check(_load().kvx_transfer_create(ctypes.byref(h)))
+        self.handle = h.value
+        self._done = _int()
+
+    def start(self, src_addrs, dst_addrs, sizes, dir, chunk_descriptors=0, launch=None, stream=None):
+        s, d, z, n = _triple(src_addrs, dst_addrs, sizes, None)
+        lp = _launch(launch)
+        _check(_load().kvx_transfer_start(self.handle, s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                          int(chunk_descriptors), ctypes.byref(lp) if lp is not None else None,
+                                          _stream(stream)))
+
+    def poll(self) -> bool:
+        """Submit the next piece if the last one completed; True once all pieces completed."""
+        _check(_load().kvx_transfer_poll(self.handle, ctypes.byref(self._done)))
+        return bool(self._done.value)
+
+    def progress(self):
+        a, b = _sz(), _sz()
+        _check(_load().kvx_transfer_progress(self.handle, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
+
+    def close(self):
+        if self.handle:
+            _check(_load().kvx_transfer_destroy(self.handle))
             self.handle = 0
 
     def __del__(self):

@@ -207,6 +207,40 @@ kvx_status kvx_copy_device_list(kvx_devlist *list, const uint64_t *d_src, const 
                                 const uint64_t *d_sizes, const uint32_t *d_count, int dir,
                                 const kvx_launch *launch, void *stream);
 
+/* ---- tail-bounded submission --------------------------------------------- */
+
+/* A transfer cut into pieces of at most chunk_descriptors descriptors, each
+ * submitted (through kvx_copy_batch_ex) only after the previous piece has
+ * completed on the GPU. This bounds how long a transfer holds SMs and link
+ * bandwidth at a time, at the cost of throughput, for serving where a
+ * colocated decode's tail latency matters (PegaFlow issue #408, follow-up §2
+ * and §Proposed direction: `chunk_descriptors` with event-based completion
+ * backpressure; enqueue-only chunking does not help). kvx never blocks: the
+ * caller's transfer worker calls kvx_transfer_poll until it reports done,
+ * yielding in between. */
+typedef struct kvx_transfer kvx_transfer;
+
+kvx_status kvx_transfer_create(kvx_transfer **out);
+
+/* Validate the whole batch (at the current validation level), take a copy of
+ * the three arrays (the caller may reuse them on return), and submit the
+ * first piece on `stream`. chunk_descriptors == 0 submits the batch as one
+ * piece. KVX_ERR_INVALID_ARG while a piece of the previous transfer is still
+ * in flight (poll it to done first). */
+kvx_status kvx_transfer_start(kvx_transfer *t, const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                              const uint64_t *sizes, size_t n, int dir, size_t chunk_descriptors,
+                              const kvx_launch *launch, void *stream);
+
+/* Non-blocking: if the piece in flight has completed, submit the next one.
+ * *done = 1 once every piece has completed. */
+kvx_status kvx_transfer_poll(kvx_transfer *t, int *done);
+
+/* Descriptors submitted so far and in total (either pointer may be NULL). */
+kvx_status kvx_transfer_progress(const kvx_transfer *t, size_t *submitted, size_t *total);
+
+/* Wait for the piece in flight, if any, and free the transfer. */
+kvx_status kvx_transfer_destroy(kvx_transfer *t);
+
 /* ---- host-only helpers (no CUDA call, no GPU needed) -------------------- */
 
 /* Validate a batch at `level` (0: arrays, dir, alignment, overflow, capacity;

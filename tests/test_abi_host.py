@@ -267,3 +267,14 @@ def test_descriptors_helper_fill_and_capacity():
     with pytest.raises(kvx.KvxError) as e:
         d.copy_batch("h2d")
     assert e.value.status == kvx.KVX_ERR_ALIGN
+
+
+def test_transfer_host_paths():
+    t = kvx.Transfer()
+    assert t.poll() is True and t.progress() == (0, 0)  # nothing started: done
+    with pytest.raises(kvx.KvxError) as e:
+        t.start([1 << 20], [1 << 30], [12], "h2d", 4)
+    assert e.value.status == kvx.KVX_ERR_ALIGN
+    t.start([], [], [], "h2d", 4)  # an empty transfer needs no device
+    assert t.poll() is True
+    t.close()
