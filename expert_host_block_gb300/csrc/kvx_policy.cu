@@ -1,0 +1,95 @@
+// Auto policy: choose DMA or the copy kernel, and the kernel's shape, from the
+// observable shape of a transfer.
+//
+// The pages propose an Auto policy "based on observable transfer shape, such
+// as merged range count, total bytes, and average range size", with separate
+// throughput-balanced and tail-bounded operating points chosen per device
+// (PegaFlow issue #408, §Discussion item 2 and follow-up §Proposed direction;
+// the vLLM report's threshold/minimum-count selection is the same idea, vLLM
+// PR #42212 report, §实现拆解 item 2). The GB300 measurements behind the rules:
+//   - per-range cudaMemcpyAsync costs about 2.6 us of host submission per
+//     range, so it loses to the kernel at every fragmented shape measured
+//     (4-64 KiB, 16-65,536 descriptors), but a range of 1 MiB or more moves at
+//     the link peak on the copy engines and occupies no SM at all;
+//   - the LDG kernel reaches the link peak fastest (throughput);
+//   - the one-warp bulk CTAs at a budget of 4 cost the colocated decode stand-in
+//     the least p99 while still sustaining a paced KV burst (tail-bounded).
+#include <cuda_runtime.h>
+
+#include "kvx_internal.h"
+
+namespace {
+
+constexpr size_t kDmaMaxRanges = 16;            // few enough ranges to submit one by one
+constexpr uint64_t kDmaMinMeanBytes = 1ull << 20;  // each long enough to hide its submission
+constexpr int kTailBudget = 4;                   // bulk CTAs of the tail-bounded policy
+
+// Number of ranges after merging descriptors that continue the previous one
+// in both source and destination (the direct path's coalescing).
+size_t merged_ranges(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                     size_t stop_after)
+{
+    size_t ranges = 0;
+    uint64_t end_s = 0, end_d = 0;
+    bool open = false;
+    for (size_t i = 0; i < n; ++i) {
+        if (!sizes[i])
+            continue;
+        if (!open || src[i] != end_s || dst[i] != end_d) {
+            if (++ranges > stop_after)
+                return ranges;
+            open = true;
+        }
+        end_s = src[i] + sizes[i];
+        end_d = dst[i] + sizes[i];
+    }
+    return ranges;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvx_status kvx_auto_path(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                         int dir, int policy, int *path)
+{
+    if (!path)
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_auto_path: null output");
+    if (policy != KVX_POLICY_THROUGHPUT && policy != KVX_POLICY_TAIL)
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_auto_path: policy is not THROUGHPUT or TAIL");
+    kvx_status st = kvx_validate(src, dst, sizes, n, dir, 0);
+    if (st != KVX_OK)
+        return st;
+    uint64_t bytes = 0;
+    for (size_t i = 0; i < n; ++i)
+        bytes += sizes[i];
+    const size_t ranges = merged_ranges(src, dst, sizes, n, kDmaMaxRanges);
+    if (ranges > 0 && ranges <= kDmaMaxRanges && bytes / ranges >= kDmaMinMeanBytes)
+        *path = KVX_PATH_DMA;
+    else
+        *path = policy == KVX_POLICY_TAIL ? KVX_PATH_KERNEL_BULK : KVX_PATH_KERNEL_LDG;
+    return KVX_OK;
+}
+
+kvx_status kvx_copy_batch_auto(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                               int dir, int policy, void *stream, int *path_out)
+{
+    int path = 0;
+    kvx_status st = kvx_auto_path(src, dst, sizes, n, dir, policy, &path);
+    if (st != KVX_OK)
+        return st;
+    if (path_out)
+        *path_out = path;
+    if (path == KVX_PATH_DMA)
+        return kvx_copy_batch_memcpy(src, dst, sizes, n, dir, stream, nullptr);
+    kvx_launch l{};
+    if (path == KVX_PATH_KERNEL_BULK) {
+        l.variant = KVX_VARIANT_BULK;
+        l.cta_budget = kTailBudget;
+    } else {
+        l.variant = KVX_VARIANT_LDG;
+    }
+    return kvx_copy_batch_ex(src, dst, sizes, n, dir, &l, stream);
+}
+
+}  // extern "C"

@@ -55,7 +55,7 @@ EXPORTS = (
     "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
     "kvx_transfer_create", "kvx_transfer_start", "kvx_transfer_poll", "kvx_transfer_progress",
-    "kvx_transfer_destroy",
+    "kvx_transfer_destroy", "kvx_auto_path", "kvx_copy_batch_auto",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
@@ -121,6 +121,8 @@ def _load():
         "kvx_transfer_poll": ([_vp, ctypes.POINTER(_int)], _int),
         "kvx_transfer_progress": ([_vp, ctypes.POINTER(_sz), ctypes.POINTER(_sz)], _int),
         "kvx_transfer_destroy": ([_vp], _int),
+        "kvx_auto_path": ([_vp, _vp, _vp, _sz, _int, _int, ctypes.POINTER(_int)], _int),
+        "kvx_copy_batch_auto": ([_vp, _vp, _vp, _sz, _int, _int, _vp, ctypes.POINTER(_int)], _int),
         "kvx_devlist_destroy": ([_vp], _int),
         "kvx_copy_device_list": ([_vp, _u64, _u64, _u64, _u64, _int, ctypes.POINTER(kvx_launch), _vp], _int),
         "kvx_standin_gemv_bf16": ([_u64, _u64, _u64, _u64, ctypes.c_uint32, _int, _vp], _int),
@@ -359,6 +361,34 @@ class DeviceList:
             self.close()
         except Exception:
             pass
+
+
+# ---- Auto policy ----------------------------------------------------------------
+
+KVX_POLICY_THROUGHPUT, KVX_POLICY_TAIL = 0, 1
+POLICIES = {"throughput": KVX_POLICY_THROUGHPUT, "tail": KVX_POLICY_TAIL}
+KVX_PATH_KERNEL_LDG, KVX_PATH_KERNEL_BULK, KVX_PATH_DMA = 1, 2, 3
+PATHS = {KVX_PATH_KERNEL_LDG: "kernel_ldg", KVX_PATH_KERNEL_BULK: "kernel_bulk", KVX_PATH_DMA: "dma"}
+
+
+def _policy(p) -> int:
+    return POLICIES[p] if isinstance(p, str) else int(p)
+
+
+def kvx_auto_path(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, policy="throughput") -> str:
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    out = _int()
+    _check(_load().kvx_auto_path(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir), _policy(policy),
+                                 ctypes.byref(out)))
+    return PATHS[out.value]
+
+
+def kvx_copy_batch_auto(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, policy="throughput", stream=None) -> str:
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    out = _int()
+    _check(_load().kvx_copy_batch_auto(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                       _policy(policy), _stream(stream), ctypes.byref(out)))
+    return PATHS[out.value]
 
 
 # ---- tail-bounded submission ---------------------------------------------------

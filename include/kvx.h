@@ -241,6 +241,28 @@ kvx_status kvx_transfer_progress(const kvx_transfer *t, size_t *submitted, size_
 /* Wait for the piece in flight, if any, and free the transfer. */
 kvx_status kvx_transfer_destroy(kvx_transfer *t);
 
+/* ---- Auto policy -------------------------------------------------------- */
+
+/* Choose the path from the transfer's shape: merged range count (descriptors
+ * that continue the previous one in both source and destination merge), total
+ * bytes and mean range size (PegaFlow issue #408, §Discussion item 2). A few
+ * large ranges (at most 16, averaging at least 1 MiB) go to the copy engines
+ * (per-range cudaMemcpyAsync: the link peak with no SM used); everything else
+ * goes to the copy kernel, the LDG variant with the calibrated budget for
+ * KVX_POLICY_THROUGHPUT, or the bulk variant with 4 one-warp CTAs for
+ * KVX_POLICY_TAIL (the lightest footprint beside a colocated decode). */
+typedef enum kvx_policy { KVX_POLICY_THROUGHPUT = 0, KVX_POLICY_TAIL = 1 } kvx_policy;
+typedef enum kvx_path { KVX_PATH_KERNEL_LDG = 1, KVX_PATH_KERNEL_BULK = 2, KVX_PATH_DMA = 3 } kvx_path;
+
+/* The path kvx_copy_batch_auto would take (host only; validation level 0). */
+kvx_status kvx_auto_path(const uint64_t *src_addrs, const uint64_t *dst_addrs, const uint64_t *sizes,
+                         size_t n, int dir, int policy, int *path);
+
+/* Copy a batch along the path kvx_auto_path chooses; *path (may be NULL)
+ * receives it. Same rules and errors as kvx_copy_batch. */
+kvx_status kvx_copy_batch_auto(const uint64_t *src_addrs, const uint64_t *dst_addrs, const uint64_t *sizes,
+                               size_t n, int dir, int policy, void *stream, int *path);
+
 /* ---- host-only helpers (no CUDA call, no GPU needed) -------------------- */
 
 /* Validate a batch at `level` (0: arrays, dir, alignment, overflow, capacity;

@@ -278,3 +278,29 @@ def test_transfer_host_paths():
     t.start([], [], [], "h2d", 4)  # an empty transfer needs no device
     assert t.poll() is True
     t.close()
+
+
+def test_auto_path_rules():
+    M = 1 << 20
+    # a few large ranges: DMA
+    assert kvx.kvx_auto_path([1 << 30], [1 << 40], [4 * M], None, "h2d") == "dma"
+    assert kvx.kvx_auto_path([1 << 30] * 1, [1 << 40], [M], None, "h2d", "tail") == "dma"
+    # adjacent descriptors merge into one large range: DMA
+    s = (1 << 30) + 4096 * np.arange(1024, dtype=np.uint64)
+    d = (1 << 40) + 4096 * np.arange(1024, dtype=np.uint64)
+    assert kvx.kvx_auto_path(s, d, np.full(1024, 4096), None, "d2d") == "dma"
+    # shuffled small descriptors: the kernel, by policy
+    g = np.random.default_rng(1)
+    s = (1 << 30) + 4096 * g.permutation(4096)[:1024].astype(np.uint64)
+    assert kvx.kvx_auto_path(s, d, np.full(1024, 4096), None, "h2d") == "kernel_ldg"
+    assert kvx.kvx_auto_path(s, d, np.full(1024, 4096), None, "h2d", "tail") == "kernel_bulk"
+    # 17 large ranges: too many to submit one by one
+    s = (1 << 30) + 2 * M * np.arange(17, dtype=np.uint64)
+    d = (1 << 40) + 2 * M * np.arange(17, dtype=np.uint64)
+    assert kvx.kvx_auto_path(s, d, np.full(17, M), None, "h2d") == "kernel_ldg"
+    # small mean: kernel
+    assert kvx.kvx_auto_path([1 << 30, 1 << 31], [1 << 40, 1 << 41], [M, 8], None, "h2d") == "kernel_ldg"
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_auto_path([1 << 30], [1 << 40], [12], None, "h2d")
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_auto_path([1 << 30], [1 << 40], [8], None, "h2d", 7)

@@ -471,3 +471,27 @@ def test_descriptors_helper_parity(level0):
         p.assert_equal(want)
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("policy", ["throughput", "tail"])
+@pytest.mark.parametrize("shape", ["few_large", "fragmented"])
+def test_auto_policy_paths(policy, shape):
+    if shape == "few_large":
+        p = _pools_small("host", "device", body=40 * W.MIB)
+        b = _batch([0, 12 * W.MIB, 30 * W.MIB], [8 * W.MIB, 20 * W.MIB, 2 * W.MIB], [4 * W.MIB, 3 * W.MIB, W.MIB],
+                   "h2d")
+        expect = "dma"
+    else:
+        w = W.sweep_cell(8, 3000, "h2d", odd_tails=True)
+        p = Pools(w.pools)
+        b = w.batches[0]
+        expect = "kernel_ldg" if policy == "throughput" else "kernel_bulk"
+    try:
+        want = p.expected([b])
+        path = kvx.kvx_copy_batch_auto(*p.addrs(b), None, "h2d", policy, None)
+        assert path == expect
+        torch.cuda.synchronize()
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
