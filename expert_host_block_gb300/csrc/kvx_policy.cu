@@ -6,23 +6,32 @@
 // throughput-balanced and tail-bounded operating points chosen per device
 // (PegaFlow issue #408, §Discussion item 2 and follow-up §Proposed direction;
 // the vLLM report's threshold/minimum-count selection is the same idea, vLLM
-// PR #42212 report, §实现拆解 item 2). The GB300 measurements behind the rules:
+// PR #42212 report, §实现拆解 item 2). The GB300 measurements behind the rules
+// (H2D, host wall clock from submission to completion):
 //   - per-range cudaMemcpyAsync costs about 2.6 us of host submission per
 //     range, so it loses to the kernel at every fragmented shape measured
-//     (4-64 KiB, 16-65,536 descriptors), but a range of 1 MiB or more moves at
-//     the link peak on the copy engines and occupies no SM at all;
-//   - the LDG kernel reaches the link peak fastest (throughput);
-//   - the one-warp bulk CTAs at a budget of 4 cost the colocated decode stand-in
-//     the least p99 while still sustaining a paced KV burst (tail-bounded).
+//     (4-64 KiB, 16-65,536 descriptors);
+//   - with few large ranges it wins: 1 x 256 KiB 10.5 vs 8.0 GB/s, 1 x 4 MiB
+//     92 vs 77, 4 x 1 MiB 82 vs 78; it ties at 16 x 4-16 MiB (180-202 vs
+//     188-203) and loses at 16 x 1 MiB (122 vs 149) and at 64 ranges. So the
+//     throughput policy takes DMA for at most 8 ranges whose mean is at least
+//     ranges x 256 KiB;
+//   - the copy engines occupy no SM at all, so the tail policy takes DMA
+//     whenever it stays near the link peak (at most 16 ranges of 1 MiB mean);
+//   - otherwise: the LDG kernel reaches the link peak fastest (throughput);
+//     the one-warp bulk CTAs at a budget of 4 cost the colocated decode
+//     stand-in the least p99 while still sustaining a paced KV burst (tail).
 #include <cuda_runtime.h>
 
 #include "kvx_internal.h"
 
 namespace {
 
-constexpr size_t kDmaMaxRanges = 16;            // few enough ranges to submit one by one
-constexpr uint64_t kDmaMinMeanBytes = 1ull << 20;  // each long enough to hide its submission
-constexpr int kTailBudget = 4;                   // bulk CTAs of the tail-bounded policy
+constexpr size_t kDmaMaxRangesThroughput = 8;         // DMA ranges, throughput policy
+constexpr uint64_t kDmaMeanPerRange = 256ull << 10;    // ... each averaging ranges x 256 KiB
+constexpr size_t kDmaMaxRangesTail = 16;               // DMA ranges, tail policy
+constexpr uint64_t kDmaMinMeanTail = 1ull << 20;       // ... averaging at least 1 MiB
+constexpr int kTailBudget = 4;                         // bulk CTAs of the tail-bounded policy
 
 // Number of ranges after merging descriptors that continue the previous one
 // in both source and destination (the direct path's coalescing).
@@ -63,8 +72,16 @@ kvx_status kvx_auto_path(const uint64_t *src, const uint64_t *dst, const uint64_
     uint64_t bytes = 0;
     for (size_t i = 0; i < n; ++i)
         bytes += sizes[i];
-    const size_t ranges = merged_ranges(src, dst, sizes, n, kDmaMaxRanges);
-    if (ranges > 0 && ranges <= kDmaMaxRanges && bytes / ranges >= kDmaMinMeanBytes)
+    const size_t ranges = merged_ranges(src, dst, sizes, n, kDmaMaxRangesTail);
+    bool dma = false;
+    if (ranges > 0) {
+        const uint64_t mean = bytes / ranges;
+        if (policy == KVX_POLICY_TAIL)
+            dma = ranges <= kDmaMaxRangesTail && mean >= kDmaMinMeanTail;
+        else
+            dma = ranges <= kDmaMaxRangesThroughput && mean >= ranges * kDmaMeanPerRange;
+    }
+    if (dma)
         *path = KVX_PATH_DMA;
     else
         *path = policy == KVX_POLICY_TAIL ? KVX_PATH_KERNEL_BULK : KVX_PATH_KERNEL_LDG;

@@ -246,11 +246,13 @@ kvx_status kvx_transfer_destroy(kvx_transfer *t);
 /* Choose the path from the transfer's shape: merged range count (descriptors
  * that continue the previous one in both source and destination merge), total
  * bytes and mean range size (PegaFlow issue #408, §Discussion item 2). A few
- * large ranges (at most 16, averaging at least 1 MiB) go to the copy engines
- * (per-range cudaMemcpyAsync: the link peak with no SM used); everything else
- * goes to the copy kernel, the LDG variant with the calibrated budget for
- * KVX_POLICY_THROUGHPUT, or the bulk variant with 4 one-warp CTAs for
- * KVX_POLICY_TAIL (the lightest footprint beside a colocated decode). */
+ * large ranges go to the copy engines (per-range cudaMemcpyAsync: near the
+ * link peak with no SM used): for KVX_POLICY_THROUGHPUT at most 8 ranges whose
+ * mean is at least ranges x 256 KiB (where DMA measured faster than the
+ * kernel), for KVX_POLICY_TAIL at most 16 ranges averaging at least 1 MiB.
+ * Everything else goes to the copy kernel: the LDG variant with the calibrated
+ * budget for THROUGHPUT, the bulk variant with 4 one-warp CTAs for TAIL (the
+ * lightest footprint beside a colocated decode). */
 typedef enum kvx_policy { KVX_POLICY_THROUGHPUT = 0, KVX_POLICY_TAIL = 1 } kvx_policy;
 typedef enum kvx_path { KVX_PATH_KERNEL_LDG = 1, KVX_PATH_KERNEL_BULK = 2, KVX_PATH_DMA = 3 } kvx_path;
 

@@ -284,7 +284,15 @@ def test_auto_path_rules():
     M = 1 << 20
     # a few large ranges: DMA
     assert kvx.kvx_auto_path([1 << 30], [1 << 40], [4 * M], None, "h2d") == "dma"
+    assert kvx.kvx_auto_path([1 << 30], [1 << 40], [256 << 10], None, "h2d") == "dma"
     assert kvx.kvx_auto_path([1 << 30] * 1, [1 << 40], [M], None, "h2d", "tail") == "dma"
+    # 16 ranges of 1 MiB: the kernel for throughput, DMA (no SMs) for the tail
+    s = (1 << 30) + 2 * M * np.arange(16, dtype=np.uint64)
+    d = (1 << 40) + 2 * M * np.arange(16, dtype=np.uint64)
+    assert kvx.kvx_auto_path(s, d, np.full(16, M), None, "h2d") == "kernel_ldg"
+    assert kvx.kvx_auto_path(s, d, np.full(16, M), None, "h2d", "tail") == "dma"
+    # 4 ranges of 1 MiB: DMA for both
+    assert kvx.kvx_auto_path(s[:4], d[:4], np.full(4, M), None, "h2d") == "dma"
     # adjacent descriptors merge into one large range: DMA
     s = (1 << 30) + 4096 * np.arange(1024, dtype=np.uint64)
     d = (1 << 40) + 4096 * np.arange(1024, dtype=np.uint64)
@@ -294,12 +302,13 @@ def test_auto_path_rules():
     s = (1 << 30) + 4096 * g.permutation(4096)[:1024].astype(np.uint64)
     assert kvx.kvx_auto_path(s, d, np.full(1024, 4096), None, "h2d") == "kernel_ldg"
     assert kvx.kvx_auto_path(s, d, np.full(1024, 4096), None, "h2d", "tail") == "kernel_bulk"
-    # 17 large ranges: too many to submit one by one
+    # 17 large ranges: too many to submit one by one, for either policy
     s = (1 << 30) + 2 * M * np.arange(17, dtype=np.uint64)
     d = (1 << 40) + 2 * M * np.arange(17, dtype=np.uint64)
     assert kvx.kvx_auto_path(s, d, np.full(17, M), None, "h2d") == "kernel_ldg"
-    # small mean: kernel
-    assert kvx.kvx_auto_path([1 << 30, 1 << 31], [1 << 40, 1 << 41], [M, 8], None, "h2d") == "kernel_ldg"
+    assert kvx.kvx_auto_path(s, d, np.full(17, M), None, "h2d", "tail") == "kernel_bulk"
+    # two ranges with a mean below 2 x 256 KiB: kernel
+    assert kvx.kvx_auto_path([1 << 30, 1 << 31], [1 << 40, 1 << 41], [256 << 10, 8], None, "h2d") == "kernel_ldg"
     with pytest.raises(kvx.KvxError):
         kvx.kvx_auto_path([1 << 30], [1 << 40], [12], None, "h2d")
     with pytest.raises(kvx.KvxError):
