@@ -30,6 +30,7 @@
 #include <vector>
 
 #include "kvx_internal.h"
+#include "kvx_workers.h"
 
 using kvx::Launch;
 
@@ -295,11 +296,15 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
 // Returns false (having written garbage) when a descriptor fails a level-0
 // check or is longer than one chunk; the caller then takes the exact two-pass
 // path, which also reports the first failing descriptor.
-bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
-               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
+struct PackAcc {
+    uint64_t bad = 0, bytes = 0, longest = 0;
+};
+
+void pack_fast_range(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t a, size_t b,
+                     kvx_chunk *out, PackAcc &acc)
 {
     uint64_t bad = 0, bytes = 0, longest = 0;
-    for (size_t i = 0; i < n; ++i) {
+    for (size_t i = a; i < b; ++i) {
         const uint64_t z = sizes[i], s = src[i], d = dst[i];
         const uint64_t live = z ? ~0ull : 0ull;
         bad |= live & (((s | d | z) & 7u) | ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d)) << 3));
@@ -308,11 +313,40 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
         longest = z > longest ? z : longest;
         out[i] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
     }
-    if (bad || n > KVX_MAX_CHUNKS)
+    acc.bad = bad;
+    acc.bytes = bytes;
+    acc.longest = longest;
+}
+
+bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
+{
+    // Large batches are split over the calling thread and the worker pool.
+    constexpr size_t kParallelMin = 8192, kMinPart = 4096;
+    constexpr int kMaxParts = 16;
+    PackAcc acc[kMaxParts];
+    int parts = 1;
+    if (n >= kParallelMin) {
+        kvx::Workers &w = kvx::Workers::get();
+        parts = std::min<int>({w.threads() + 1, kMaxParts, (int)(n / kMinPart)});
+        if (parts > 1 && !w.run(parts, [&](int p) {
+                pack_fast_range(src, dst, sizes, n * p / parts, n * (p + 1) / parts, out, acc[p]);
+            }))
+            parts = 1;
+    }
+    if (parts == 1)
+        pack_fast_range(src, dst, sizes, 0, n, out, acc[0]);
+    PackAcc t;
+    for (int p = 0; p < parts; ++p) {
+        t.bad |= acc[p].bad;
+        t.bytes += acc[p].bytes;
+        t.longest = std::max(t.longest, acc[p].longest);
+    }
+    if (t.bad || n > KVX_MAX_CHUNKS)
         return false;
     *n_chunks = n;
-    *payload = bytes;
-    *max_chunk = (uint32_t)longest;
+    *payload = t.bytes;
+    *max_chunk = (uint32_t)t.longest;
     return true;
 }
 
