@@ -404,8 +404,8 @@ kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch 
             return fail(KVX_ERR_INVALID_ARG, "threads %d is not 128, 256 or 512", want->threads);
         if (want->unroll && want->unroll != 2 && want->unroll != 4 && want->unroll != 8)
             return fail(KVX_ERR_INVALID_ARG, "unroll %d is not 2, 4 or 8", want->unroll);
-        if (want->stages && (want->stages < 2 || want->stages > 4))
-            return fail(KVX_ERR_INVALID_ARG, "stages %d is not in 2..4", want->stages);
+        if (want->stages && (want->stages < 2 || want->stages > 12))
+            return fail(KVX_ERR_INVALID_ARG, "stages %d is not in 2..12", want->stages);
         if (want->store_policy < 0 || want->store_policy > 2)
             return fail(KVX_ERR_INVALID_ARG, "store_policy %d is not 0, 1 or 2", want->store_policy);
     }

@@ -35,7 +35,7 @@ struct Launch {
     int ctas;          // grid size (already clamped to the work)
     int threads;       // LDG threads per CTA
     int unroll;        // LDG 16-byte loads in flight per lane
-    int stages;        // BULK ring stages
+    int stages;        // BULK ring size in units of KVX_CHUNK_BYTES
     int store_policy;  // LDG store cache policy
 };
 
@@ -65,7 +65,7 @@ kvx_status set_error(kvx_status status, const char *message);
 // Enqueue the bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
 
-// Shared memory the bulk kernel needs for `stages` stages.
-size_t bulk_smem_bytes(int stages);
+// Shared memory of a bulk ring of `units` x KVX_CHUNK_BYTES.
+size_t bulk_smem_bytes(int units);
 
 }  // namespace kvx

@@ -15,11 +15,13 @@
 // reads the records of its next 32 chunks with one load per lane and passes
 // them around with shuffles, so no lane waits on a record load per chunk.
 //
-// BULK variant: one warp per CTA; lane 0 streams chunks through an S-stage
-// ring of 16 KiB shared::cta buffers with cp.async.bulk loads completed on an
-// mbarrier, then cp.async.bulk stores (FreeToken issue #751, §What we changed:
-// a 3-stage ring, one issuing thread per CTA, the .shared::cta destination
-// form). Every mbarrier wait is bounded by %globaltimer.
+// BULK variant: one warp per CTA; lane 0 streams chunks through a ring of
+// shared::cta stages with cp.async.bulk loads completed on an mbarrier, then
+// cp.async.bulk stores (FreeToken issue #751, §What we changed: a 3-stage
+// ring of 16 KiB, one issuing thread per CTA, the .shared::cta destination
+// form). Here a stage is as large as the batch's longest chunk, so a ring of
+// 4 KiB chunks has many more stages, and loads, in flight than one of 16 KiB
+// chunks. Every mbarrier wait is bounded by %globaltimer.
 //
 // Unaligned pieces: addresses and sizes are multiples of 8. When src and dst
 // have the same phase mod 16, a chunk is an 8-byte head, a 16-byte-word body
@@ -383,18 +385,23 @@ __device__ __forceinline__ bool bulk_ok(const Rec &r)
     return r.l != 0 && ((r.s | r.d | (uint64_t)r.l) & 15u) == 0;
 }
 
-template <int S>
+constexpr int kBulkMaxStages = 32;
+
+// The ring is `S` stages of `stage` bytes (the batch's longest chunk rounded
+// up to 16 bytes), so small chunks get many stages: S - 1 loads stay in
+// flight per CTA.
 __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__restrict__ tab,
-                                                           uint32_t n_chunks, uint64_t wait_ns)
+                                                           uint32_t n_chunks, uint32_t stage,
+                                                           uint32_t S, uint64_t wait_ns)
 {
     extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t bars[S];
+    __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
     const uint32_t lane = threadIdx.x;
     const uint32_t ring0 = smem_u32(ring);
     const uint32_t bar0 = smem_u32(bars);
 
     if (lane == 0) {
-        for (int s = 0; s < S; ++s)
+        for (uint32_t s = 0; s < S; ++s)
             mbar_init(bar0 + 8u * s, 1);
         mbar_init_fence();
     }
@@ -410,7 +417,8 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             r = load_rec(tab, chunk_of(k0 + lane));
         return r;
     };
-    // Records of chunks [a0, a0+32) in batch A and [a0+32, a0+64) in batch B.
+    // Records of chunks [a0, a0+32) in batch A and [a0+32, a0+64) in batch B;
+    // the look-ahead k + S - 1 stays below a0 + 64 because S <= 32.
     uint64_t a0 = 0;
     Rec A = load_batch(0);
     Rec B = load_batch(32);
@@ -424,13 +432,13 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     uint32_t pending = 0;  // bit s: a load is in flight on stage s
     bool timed_out = false;
 
-    for (int j = 0; j < S - 1; ++j) {  // prologue: fill S-1 stages
+    for (uint32_t j = 0; j + 1 < S; ++j) {  // prologue: fill S-1 stages
         if ((uint64_t)j < my_n) {
             const Rec r = fetch(j);
             if (bulk_ok(r)) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar0 + 8u * j, r.l);
-                    bulk_load(ring0 + (uint32_t)j * KVX_CHUNK_BYTES, r.s, r.l, bar0 + 8u * j);
+                    bulk_load(ring0 + j * stage, r.s, r.l, bar0 + 8u * j);
                 }
                 pending |= 1u << j;
             }
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             B = load_batch(a0 + 32);
         }
         const Rec r = fetch(k);
-        const int st = (int)(k % S);
+        const uint32_t st = (uint32_t)(k % S);
         bool stored = false;
         if (bulk_ok(r)) {
             // Lane 0 waits; the outcome is broadcast so the warp stays converged.
@@ -458,7 +466,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             phase ^= 1u << st;
             pending &= ~(1u << st);
             if (lane == 0) {
-                bulk_store(r.d, ring0 + (uint32_t)st * KVX_CHUNK_BYTES, r.l);
+                bulk_store(r.d, ring0 + st * stage, r.l);
                 bulk_commit();
             }
             stored = true;
@@ -469,14 +477,14 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
         if (j < my_n) {
             const Rec n = fetch(j);
             if (bulk_ok(n)) {
-                const int sj = (int)(j % S);  // == (k - 1) mod S: the stage chunk k-1 used
+                const uint32_t sj = (uint32_t)(j % S);  // == (k - 1) mod S: the stage chunk k-1 used
                 if (lane == 0) {
                     if (stored)
                         bulk_wait_read<1>();
                     else
                         bulk_wait_read<0>();
                     mbar_arrive_expect_tx(bar0 + 8u * sj, n.l);
-                    bulk_load(ring0 + (uint32_t)sj * KVX_CHUNK_BYTES, n.s, n.l, bar0 + 8u * sj);
+                    bulk_load(ring0 + sj * stage, n.s, n.l, bar0 + 8u * sj);
                 }
                 pending |= 1u << sj;
             }
@@ -488,7 +496,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             atomicOr(&g_status, kDevErrTimeout);
         // Let the loads still in flight land before the shared memory goes away.
         if (lane == 0)
-            for (int s = 0; s < S; ++s)
+            for (uint32_t s = 0; s < S; ++s)
                 if (pending & (1u << s))
                     mbar_wait_bounded(bar0 + 8u * s, (phase >> s) & 1u, wait_ns);
     }
@@ -690,15 +698,21 @@ cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint3
     }
 }
 
-template <int S>
-cudaError_t launch_bulk(int ctas, const kvx_chunk *t, uint32_t n, cudaStream_t s)
+cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n, uint32_t max_chunk_len,
+                        cudaStream_t s)
 {
-    const size_t smem = bulk_smem_bytes(S);
-    cudaError_t e = cudaFuncSetAttribute(kvx_copy_bulk_kernel<S>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const uint32_t ring = (uint32_t)bulk_smem_bytes(ring_units);
+    uint32_t stage = (max_chunk_len + 15u) & ~15u;
+    if (stage < 16u)
+        stage = 16u;
+    uint32_t S = ring / stage;
+    if (S > (uint32_t)kBulkMaxStages)
+        S = kBulkMaxStages;
+    cudaError_t e = cudaFuncSetAttribute(kvx_copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)ring);
     if (e != cudaSuccess)
         return e;
-    kvx_copy_bulk_kernel<S><<<ctas, 32, smem, s>>>(t, n, kBulkWaitNs);
+    kvx_copy_bulk_kernel<<<ctas, 32, ring, s>>>(t, n, stage, S, kBulkWaitNs);
     return cudaGetLastError();
 }
 
@@ -747,11 +761,7 @@ cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chun
         return cudaSuccess;
     const int ctas = work_ctas(l, n_chunks, max_chunk_len);
     if (l.variant == KVX_VARIANT_BULK) {
-        switch (l.stages) {
-        case 2: return launch_bulk<2>(ctas, table, n_chunks, stream);
-        case 4: return launch_bulk<4>(ctas, table, n_chunks, stream);
-        default: return launch_bulk<3>(ctas, table, n_chunks, stream);
-        }
+        return launch_bulk(ctas, l.stages, table, n_chunks, max_chunk_len, stream);
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
     switch (l.unroll) {

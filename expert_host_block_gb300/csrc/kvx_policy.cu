@@ -32,6 +32,7 @@ constexpr uint64_t kDmaMeanPerRange = 256ull << 10;    // ... each averaging ran
 constexpr size_t kDmaMaxRangesTail = 16;               // DMA ranges, tail policy
 constexpr uint64_t kDmaMinMeanTail = 1ull << 20;       // ... averaging at least 1 MiB
 constexpr int kTailBudget = 4;                         // bulk CTAs of the tail-bounded policy
+constexpr int kTailRing = 12;                          // ... each with a 192 KiB ring
 
 // Number of ranges after merging descriptors that continue the previous one
 // in both source and destination (the direct path's coalescing).
@@ -103,6 +104,7 @@ kvx_status kvx_copy_batch_auto(const uint64_t *src, const uint64_t *dst, const u
     if (path == KVX_PATH_KERNEL_BULK) {
         l.variant = KVX_VARIANT_BULK;
         l.cta_budget = kTailBudget;
+        l.stages = kTailRing;
     } else {
         l.variant = KVX_VARIANT_LDG;
     }

@@ -110,7 +110,8 @@ typedef struct kvx_launch {
     int cta_budget;      /* maximum CTAs; the grid is min(cta_budget, work) */
     int threads;         /* LDG: threads per CTA, one of 128, 256, 512 */
     int unroll;          /* LDG: 16-byte loads in flight per lane, one of 2, 4, 8 */
-    int stages;          /* BULK: ring stages of KVX_CHUNK_BYTES each, 2..4 */
+    int stages;          /* BULK: shared-memory ring of stages x KVX_CHUNK_BYTES, 2..12; it is cut
+                            into stages of the batch's longest chunk (at most 32 stages) */
     int store_policy;    /* LDG: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
 } kvx_launch;
 

@@ -215,7 +215,7 @@ def test_copy_batch_rejects_before_any_cuda_call():
 
 
 @pytest.mark.parametrize("launch", [
-    {"variant": 3}, {"threads": 1024}, {"threads": 96}, {"unroll": 3}, {"stages": 5},
+    {"variant": 3}, {"threads": 1024}, {"threads": 96}, {"unroll": 3}, {"stages": 13},
     {"store_policy": 3}, {"cta_budget": -2},
 ])
 def test_copy_batch_ex_rejects_bad_launch(launch):

@@ -44,7 +44,7 @@ def _random_case(seed):
         launch.update(threads=int(g.choice([128, 256, 512])), unroll=int(g.choice([2, 4, 8])),
                       store_policy=int(g.integers(0, 3)))
     else:
-        launch["stages"] = int(g.integers(2, 5))
+        launch["stages"] = int(g.integers(2, 13))
     ws = "host" if direction == "h2d" else "device"
     wd = "host" if direction == "d2h" else "device"
     specs = {"src": W.PoolSpec("src", ws, body, "random", (77, seed)),

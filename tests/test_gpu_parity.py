@@ -51,7 +51,9 @@ def _one(pools, batch, **kw):
                                     {"variant": "bulk", "cta_budget": 1},
                                     {"variant": "bulk", "cta_budget": 4},
                                     {"variant": "bulk", "cta_budget": 32, "stages": 2},
-                                    {"variant": "bulk", "cta_budget": 8, "stages": 4}])
+                                    {"variant": "bulk", "cta_budget": 8, "stages": 4},
+                                    {"variant": "bulk", "cta_budget": 4, "stages": 12},
+                                    {"variant": "bulk", "cta_budget": 1, "stages": 7}])
 def test_tiny_h2d(launch):
     w = W.tiny_h2d()
     p = Pools(w.pools)
@@ -493,5 +495,19 @@ def test_auto_policy_paths(policy, shape):
         torch.cuda.synchronize()
         kvx.kvx_stream_check(None)
         p.assert_equal(want)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("stages", [2, 5, 12])
+@pytest.mark.parametrize("size_kib", [4, 12, 64])
+def test_bulk_ring_sizes_with_mixed_alignment(stages, size_kib):
+    """Rings cut into stages of the longest chunk; odd-tail chunks mixed in go through the warp path."""
+    w = W.sweep_cell(size_kib, 700, "h2d", odd_tails=True)
+    (b,) = w.batches
+    b.sizes[::3] = size_kib * W.KIB  # a third of the descriptors 16-byte clean again (where aligned)
+    p = Pools(w.pools)
+    try:
+        _one(p, b, launch={"variant": "bulk", "cta_budget": 5, "stages": stages})
     finally:
         p.close()
