@@ -375,6 +375,24 @@ __device__ __forceinline__ void bulk_wait_read()
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// wait_group.read takes an immediate: dispatch a runtime count in 0..31.
+__device__ __noinline__ void bulk_wait_read_n(uint32_t n)
+{
+#define KVX_WAIT_CASE(i) \
+    case i: bulk_wait_read<i>(); return;
+    switch (n) {
+        KVX_WAIT_CASE(0) KVX_WAIT_CASE(1) KVX_WAIT_CASE(2) KVX_WAIT_CASE(3) KVX_WAIT_CASE(4)
+        KVX_WAIT_CASE(5) KVX_WAIT_CASE(6) KVX_WAIT_CASE(7) KVX_WAIT_CASE(8) KVX_WAIT_CASE(9)
+        KVX_WAIT_CASE(10) KVX_WAIT_CASE(11) KVX_WAIT_CASE(12) KVX_WAIT_CASE(13) KVX_WAIT_CASE(14)
+        KVX_WAIT_CASE(15) KVX_WAIT_CASE(16) KVX_WAIT_CASE(17) KVX_WAIT_CASE(18) KVX_WAIT_CASE(19)
+        KVX_WAIT_CASE(20) KVX_WAIT_CASE(21) KVX_WAIT_CASE(22) KVX_WAIT_CASE(23) KVX_WAIT_CASE(24)
+        KVX_WAIT_CASE(25) KVX_WAIT_CASE(26) KVX_WAIT_CASE(27) KVX_WAIT_CASE(28) KVX_WAIT_CASE(29)
+        KVX_WAIT_CASE(30)
+    default: bulk_wait_read<31>(); return;
+    }
+#undef KVX_WAIT_CASE
+}
+
 __device__ __forceinline__ void bulk_wait_all()
 {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -388,8 +406,14 @@ __device__ __forceinline__ bool bulk_ok(const Rec &r)
 constexpr int kBulkMaxStages = 32;
 
 // The ring is `S` stages of `stage` bytes (the batch's longest chunk rounded
-// up to 16 bytes), so small chunks get many stages: S - 1 loads stay in
-// flight per CTA.
+// up to 16 bytes). A bulk store's shared-memory read counts as done only once
+// its writes are accepted, so a stage cannot be refilled right after its
+// store is issued without waiting a full write latency. The ring is therefore
+// split: loads run D = S/2 chunks ahead of the chunk being stored, and up to
+// S - D stores stay in flight behind it. Every iteration commits exactly one
+// bulk group (a store, or an empty group for a chunk moved by the warp), so
+// "the store of the chunk that last used stage s" is always the group S - D
+// commits back.
 __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__restrict__ tab,
                                                            uint32_t n_chunks, uint32_t stage,
                                                            uint32_t S, uint64_t wait_ns)
@@ -399,6 +423,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     const uint32_t lane = threadIdx.x;
     const uint32_t ring0 = smem_u32(ring);
     const uint32_t bar0 = smem_u32(bars);
+    const uint32_t D = S / 2;  // loads ahead, >= 1 because S >= 2
 
     if (lane == 0) {
         for (uint32_t s = 0; s < S; ++s)
@@ -418,7 +443,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
         return r;
     };
     // Records of chunks [a0, a0+32) in batch A and [a0+32, a0+64) in batch B;
-    // the look-ahead k + S - 1 stays below a0 + 64 because S <= 32.
+    // the look-ahead k + D stays below a0 + 64 because D < 32.
     uint64_t a0 = 0;
     Rec A = load_batch(0);
     Rec B = load_batch(32);
@@ -432,7 +457,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     uint32_t pending = 0;  // bit s: a load is in flight on stage s
     bool timed_out = false;
 
-    for (uint32_t j = 0; j + 1 < S; ++j) {  // prologue: fill S-1 stages
+    for (uint32_t j = 0; j < D; ++j) {  // prologue: D loads ahead
         if ((uint64_t)j < my_n) {
             const Rec r = fetch(j);
             if (bulk_ok(r)) {
@@ -453,7 +478,6 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
         }
         const Rec r = fetch(k);
         const uint32_t st = (uint32_t)(k % S);
-        bool stored = false;
         if (bulk_ok(r)) {
             // Lane 0 waits; the outcome is broadcast so the warp stays converged.
             bool ok = true;
@@ -465,24 +489,21 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             }
             phase ^= 1u << st;
             pending &= ~(1u << st);
-            if (lane == 0) {
+            if (lane == 0)
                 bulk_store(r.d, ring0 + st * stage, r.l);
-                bulk_commit();
-            }
-            stored = true;
         } else {
             copy_chunk_warp<4, 0>(r.s, r.d, r.l, lane);
         }
-        const uint64_t j = k + S - 1;
+        if (lane == 0)
+            bulk_commit();  // one group per iteration, empty for a warp-moved chunk
+        const uint64_t j = k + D;
         if (j < my_n) {
             const Rec n = fetch(j);
             if (bulk_ok(n)) {
-                const uint32_t sj = (uint32_t)(j % S);  // == (k - 1) mod S: the stage chunk k-1 used
+                // Stage j % S last held chunk j - S, whose group is S - D commits back.
+                const uint32_t sj = (uint32_t)(j % S);
                 if (lane == 0) {
-                    if (stored)
-                        bulk_wait_read<1>();
-                    else
-                        bulk_wait_read<0>();
+                    bulk_wait_read_n(S - D);
                     mbar_arrive_expect_tx(bar0 + 8u * sj, n.l);
                     bulk_load(ring0 + sj * stage, n.s, n.l, bar0 + 8u * sj);
                 }

@@ -32,7 +32,8 @@ constexpr uint64_t kDmaMeanPerRange = 256ull << 10;    // ... each averaging ran
 constexpr size_t kDmaMaxRangesTail = 16;               // DMA ranges, tail policy
 constexpr uint64_t kDmaMinMeanTail = 1ull << 20;       // ... averaging at least 1 MiB
 constexpr int kTailBudget = 4;                         // bulk CTAs of the tail-bounded policy
-constexpr int kTailRing = 12;                          // ... each with a 192 KiB ring
+constexpr int kTailRing = 3;                           // ... each with a 48 KiB ring (a bigger ring
+                                                       // takes shared memory a colocated kernel needs)
 
 // Number of ranges after merging descriptors that continue the previous one
 // in both source and destination (the direct path's coalescing).
