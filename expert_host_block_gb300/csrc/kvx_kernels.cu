@@ -334,9 +334,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for phase `parity` of the mbarrier to complete, giving up after
-// limit_ns of %globaltimer (or 2^28 polls, whichever comes first).
-__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+// limit_ns of %globaltimer (or 2^28 polls, whichever comes first). The timer
+// is read only once a poll has failed: a phase that has already completed
+// costs one try_wait.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
+    if (mbar_try_wait(bar, parity))
+        return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0; it < (1u << 28); ++it) {
         if (mbar_try_wait(bar, parity))
