@@ -424,6 +424,10 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
 {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
+    // The record window: chunks [a0, a0 + 64) in slots c & 63. The issuing lane
+    // reads records from here; the warp fills it 32 records at a time.
+    __shared__ uint64_t w_src[64], w_dst[64];
+    __shared__ uint32_t w_len[64];
     const uint32_t lane = threadIdx.x;
     const uint32_t ring0 = smem_u32(ring);
     const uint32_t bar0 = smem_u32(bars);
@@ -434,55 +438,56 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             mbar_init(bar0 + 8u * s, 1);
         mbar_init_fence();
     }
-    __syncwarp();
 
     // Chunks of this CTA: blockIdx.x + k * gridDim.x, k in [0, my_n).
     const uint64_t my_n =
         n_chunks > blockIdx.x ? (n_chunks - 1ull - blockIdx.x) / gridDim.x + 1ull : 0ull;
-    auto chunk_of = [&](uint64_t k) { return (uint64_t)blockIdx.x + k * gridDim.x; };
+    // Load records [k0, k0 + 32) into the window; return the batch's bulk-eligibility bits.
     auto load_batch = [&](uint64_t k0) {
         Rec r = {0, 0, 0};
         if (k0 + lane < my_n)
-            r = load_rec(tab, chunk_of(k0 + lane));
-        return r;
+            r = load_rec(tab, (uint64_t)blockIdx.x + (k0 + lane) * gridDim.x);
+        const uint32_t slot = (uint32_t)((k0 + lane) & 63u);
+        w_src[slot] = r.s;
+        w_dst[slot] = r.d;
+        w_len[slot] = r.l;
+        return __ballot_sync(kFull, bulk_ok(r));
     };
-    // Records of chunks [a0, a0+32) in batch A and [a0+32, a0+64) in batch B;
-    // the look-ahead k + D stays below a0 + 64 because D < 32.
     uint64_t a0 = 0;
-    Rec A = load_batch(0);
-    Rec B = load_batch(32);
-    auto fetch = [&](uint64_t k) {
-        const Rec x = shfl_rec(A, (int)((k - a0) & 31u));
-        const Rec y = shfl_rec(B, (int)((k - a0) & 31u));
-        return (k - a0 < 32u) ? x : y;
+    uint32_t mask_a = load_batch(0);   // chunks [a0, a0 + 32)
+    uint32_t mask_b = load_batch(32);  // chunks [a0 + 32, a0 + 64); the look-ahead k + D < a0 + 64
+    __syncwarp();
+    auto eligible = [&](uint64_t c) {
+        const uint64_t o = c - a0;
+        return ((o < 32u ? mask_a >> o : mask_b >> (o - 32u)) & 1u) != 0;
     };
 
     uint32_t phase = 0;    // bit s: parity of the next completion of stage s
     uint32_t pending = 0;  // bit s: a load is in flight on stage s
     bool timed_out = false;
 
-    for (uint32_t j = 0; j < D; ++j) {  // prologue: D loads ahead
-        if ((uint64_t)j < my_n) {
-            const Rec r = fetch(j);
-            if (bulk_ok(r)) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar0 + 8u * j, r.l);
-                    bulk_load(ring0 + j * stage, r.s, r.l, bar0 + 8u * j);
-                }
-                pending |= 1u << j;
+    for (uint32_t j = 0; j < D && j < my_n; ++j) {  // prologue: D loads ahead
+        if (eligible(j)) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar0 + 8u * j, w_len[j & 63u]);
+                bulk_load(ring0 + j * stage, w_src[j & 63u], w_len[j & 63u], bar0 + 8u * j);
             }
+            pending |= 1u << j;
         }
     }
 
+    uint32_t st = 0;      // stage of chunk k: k mod S
+    uint32_t sj = D % S;  // stage of chunk k + D
     for (uint64_t k = 0; k < my_n; ++k) {
-        if (k == a0 + 32) {  // slide the record window
-            A = B;
+        if (k == a0 + 32) {  // slide the window: records [a0 + 64, a0 + 96) replace [a0, a0 + 32)
+            __syncwarp();
+            mask_a = mask_b;
+            mask_b = load_batch(a0 + 64);
             a0 += 32;
-            B = load_batch(a0 + 32);
+            __syncwarp();
         }
-        const Rec r = fetch(k);
-        const uint32_t st = (uint32_t)(k % S);
-        if (bulk_ok(r)) {
+        const uint32_t slot = (uint32_t)(k & 63u);
+        if (eligible(k)) {
             // Lane 0 waits; the outcome is broadcast so the warp stays converged.
             bool ok = true;
             if (lane == 0)
@@ -494,26 +499,25 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
             phase ^= 1u << st;
             pending &= ~(1u << st);
             if (lane == 0)
-                bulk_store(r.d, ring0 + st * stage, r.l);
+                bulk_store(w_dst[slot], ring0 + st * stage, w_len[slot]);
         } else {
-            copy_chunk_warp<4, 0>(r.s, r.d, r.l, lane);
+            copy_chunk_warp<4, 0>(w_src[slot], w_dst[slot], w_len[slot], lane);
         }
         if (lane == 0)
             bulk_commit();  // one group per iteration, empty for a warp-moved chunk
         const uint64_t j = k + D;
-        if (j < my_n) {
-            const Rec n = fetch(j);
-            if (bulk_ok(n)) {
-                // Stage j % S last held chunk j - S, whose group is S - D commits back.
-                const uint32_t sj = (uint32_t)(j % S);
-                if (lane == 0) {
-                    bulk_wait_read_n(S - D);
-                    mbar_arrive_expect_tx(bar0 + 8u * sj, n.l);
-                    bulk_load(ring0 + sj * stage, n.s, n.l, bar0 + 8u * sj);
-                }
-                pending |= 1u << sj;
+        if (j < my_n && eligible(j)) {
+            // Stage sj last held chunk j - S, whose group is S - D commits back.
+            if (lane == 0) {
+                const uint32_t js = (uint32_t)(j & 63u);
+                bulk_wait_read_n(S - D);
+                mbar_arrive_expect_tx(bar0 + 8u * sj, w_len[js]);
+                bulk_load(ring0 + sj * stage, w_src[js], w_len[js], bar0 + 8u * sj);
             }
+            pending |= 1u << sj;
         }
+        st = st + 1 == S ? 0 : st + 1;
+        sj = sj + 1 == S ? 0 : sj + 1;
     }
 
     if (timed_out) {
