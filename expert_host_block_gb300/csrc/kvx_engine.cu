@@ -360,10 +360,12 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // link from about 512 KiB in flight (8 CTAs x 512 threads x 8 x 16 B) up to
 // the whole GPU, while H2D and D2H running together peak at about 2 MiB in
 // flight per direction (64 CTAs x 256 threads) and lose throughput beyond it,
-// as the pages saw PCIe collapse past its optimum. The LDG variant reached the
-// link peak in every measured size class with fewer CTAs than the bulk ring,
-// so every row picks it. D2D fills the GPU: one 512-thread CTA per SM (about
-// 120 registers a thread leave room for one).
+// as the pages saw PCIe collapse past its optimum; LDG holds the link peak in
+// every size class there. D2D of small chunks fills the GPU with LDG (one
+// 512-thread CTA per SM: about 120 registers a thread leave room for one); of
+// chunks averaging 12 KiB or more, the bulk ring measured faster (3.28-3.36
+// TB/s of payload with 608 one-warp CTAs and 96 KiB rings, against 3.24 for
+// LDG), so that size class picks it.
 struct TableRow {
     int dir;
     uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
@@ -373,7 +375,8 @@ struct TableRow {
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0}},
+    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 608, 256, 8, 6, 0}},
 };
 
 kvx_launch table_launch(int dir, uint64_t mean_chunk)

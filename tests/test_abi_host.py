@@ -231,7 +231,7 @@ def test_default_launch_table():
             l = kvx.kvx_default_launch(dname, mean)
             assert l["variant"] in (kvx.KVX_VARIANT_LDG, kvx.KVX_VARIANT_BULK)
             assert l["cta_budget"] > 0 and l["threads"] in (128, 256, 512)
-            assert l["unroll"] in (2, 4, 8) and 2 <= l["stages"] <= 4
+            assert l["unroll"] in (2, 4, 8) and 2 <= l["stages"] <= 12
     with pytest.raises(kvx.KvxError):
         kvx.kvx_default_launch(5, 4096)
 
