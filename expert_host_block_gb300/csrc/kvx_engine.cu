@@ -986,12 +986,28 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
         return fail(KVX_ERR_ALIGN, "device arrays must be 8-byte aligned (the count 4-byte aligned)");
     if (dir < KVX_H2D || dir > KVX_D2D)
         return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
+    // Device lists are copied by the LDG variant: start from the table's LDG
+    // row for the direction (its small-chunk row) and apply the caller's fields.
+    if (want && want->variant && want->variant != KVX_VARIANT_LDG)
+        return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
+    kvx_launch merged = table_launch(dir, 0);
+    if (want) {
+        if (want->cta_budget < 0)
+            return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", want->cta_budget);
+        if (want->cta_budget)
+            merged.cta_budget = want->cta_budget;
+        if (want->threads)
+            merged.threads = want->threads;
+        if (want->unroll)
+            merged.unroll = want->unroll;
+        if (want->store_policy)
+            merged.store_policy = want->store_policy;
+    }
+    merged.variant = KVX_VARIANT_LDG;
     Launch lc;
-    st = resolve(dir, KVX_CHUNK_BYTES, want, &lc);
+    st = resolve(dir, 0, &merged, &lc);
     if (st != KVX_OK)
         return st;
-    if (lc.variant != KVX_VARIANT_LDG)
-        return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
     bool cap = false;
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
