@@ -41,6 +41,8 @@ namespace {
 
 thread_local std::string t_err;
 
+int log_level();
+
 kvx_status fail(kvx_status s, const char *fmt, ...)
 {
     char buf[512];
@@ -49,6 +51,8 @@ kvx_status fail(kvx_status s, const char *fmt, ...)
     vsnprintf(buf, sizeof buf, fmt, ap);
     va_end(ap);
     t_err = buf;
+    if (log_level() >= 1)
+        fprintf(stderr, "kvx: status %d: %s\n", (int)s, buf);
     return s;
 }
 
@@ -69,12 +73,64 @@ kvx_status cuda_fail(cudaError_t e, const char *what)
 // typo cannot silently select a default: FreeToken issue #751, §What we
 // changed, on its own switch)
 // ---------------------------------------------------------------------------
+struct TableRow {
+    int dir;
+    uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
+    kvx_launch cfg;
+};
+
 struct EnvSettings {
     int validate = 0;
     int variant = KVX_VARIANT_AUTO;
     int cta_budget = 0;
+    int log = 0;
+    std::vector<TableRow> table;  // KVX_TABLE rows, consulted before the built-in table
     std::string error;
 };
+
+// A launch table in a text file: one row per line, `#` starts a comment:
+//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy
+// with dir h2d|d2h|d2d, max_mean_chunk_bytes an integer or "inf", variant
+// ldg|bulk. Rows are tried in file order, before the built-in rows.
+std::string parse_table(const char *path, std::vector<TableRow> *rows)
+{
+    FILE *f = fopen(path, "r");
+    if (!f)
+        return std::string("KVX_TABLE=") + path + ": cannot open";
+    char line[512];
+    int lineno = 0;
+    std::string err;
+    while (err.empty() && fgets(line, sizeof line, f)) {
+        ++lineno;
+        if (char *h = strchr(line, '#'))
+            *h = 0;
+        char dir[16], maxs[32], var[16];
+        int budget, threads, unroll, stages, policy;
+        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d", dir, maxs, var, &budget, &threads,
+                               &unroll, &stages, &policy);
+        if (got <= 0)
+            continue;  // blank or comment
+        TableRow r{};
+        char *end = nullptr;
+        r.dir = !strcmp(dir, "h2d") ? KVX_H2D : !strcmp(dir, "d2h") ? KVX_D2H : !strcmp(dir, "d2d") ? KVX_D2D : -1;
+        if (!strcmp(maxs, "inf"))
+            r.max_mean_chunk = ~0ull;
+        else
+            r.max_mean_chunk = strtoull(maxs, &end, 10);
+        const int variant = !strcmp(var, "ldg") ? KVX_VARIANT_LDG : !strcmp(var, "bulk") ? KVX_VARIANT_BULK : -1;
+        if (got != 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
+            (threads != 128 && threads != 256 && threads != 512) || (unroll != 2 && unroll != 4 && unroll != 8) ||
+            stages < 2 || stages > 12 || policy < 0 || policy > 2) {
+            err = std::string("KVX_TABLE=") + path + ": line " + std::to_string(lineno) +
+                  " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy'";
+            break;
+        }
+        r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy};
+        rows->push_back(r);
+    }
+    fclose(f);
+    return err;
+}
 
 const EnvSettings &env()
 {
@@ -105,10 +161,23 @@ const EnvSettings &env()
             else
                 e.cta_budget = (int)b;
         }
+        if (const char *v = getenv("KVX_LOG")) {
+            if (strlen(v) == 1 && v[0] >= '0' && v[0] <= '2')
+                e.log = v[0] - '0';
+            else
+                e.error = std::string("KVX_LOG=") + v + " is not 0, 1 or 2";
+        }
+        if (const char *v = getenv("KVX_TABLE")) {
+            std::string err = parse_table(v, &e.table);
+            if (!err.empty())
+                e.error = err;
+        }
         return e;
     }();
     return s;
 }
+
+int log_level() { return env().log; }
 
 std::atomic<int> g_validate_level{-1};
 
@@ -366,12 +435,6 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // chunks averaging 12 KiB or more, the bulk ring measured faster (3.28-3.36
 // TB/s of payload with 608 one-warp CTAs and 96 KiB rings, against 3.24 for
 // LDG), so that size class picks it.
-struct TableRow {
-    int dir;
-    uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
-    kvx_launch cfg;
-};
-
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
@@ -381,6 +444,9 @@ const TableRow kTable[] = {
 
 kvx_launch table_launch(int dir, uint64_t mean_chunk)
 {
+    for (const TableRow &r : env().table)  // KVX_TABLE rows first
+        if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
+            return r.cfg;
     for (const TableRow &r : kTable)
         if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
             return r.cfg;
@@ -421,6 +487,15 @@ kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch 
     out->stages = stages;
     out->store_policy = policy;
     return KVX_OK;
+}
+
+void log_batch(const char *entry, int dir, size_t n, uint64_t chunks, uint64_t bytes, const Launch &l)
+{
+    if (log_level() >= 2)
+        fprintf(stderr, "kvx: %s dir=%d n=%zu chunks=%llu bytes=%llu variant=%d ctas=%d threads=%d unroll=%d "
+                        "stages=%d\n",
+                entry, dir, n, (unsigned long long)chunks, (unsigned long long)bytes, l.variant, l.ctas,
+                l.threads, l.unroll, l.stages);
 }
 
 kvx_status is_capturing(cudaStream_t stream, bool *cap)
@@ -584,6 +659,7 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
         return KVX_OK;
     }
     *done = true;
+    log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
     cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
                                     cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) {
@@ -741,6 +817,7 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     if (st != KVX_OK)
         return st;
     pack(src, dst, sizes, n, s->host);
+    log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
     cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
                                     cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) {

@@ -313,3 +313,57 @@ def test_auto_path_rules():
         kvx.kvx_auto_path([1 << 30], [1 << 40], [12], None, "h2d")
     with pytest.raises(kvx.KvxError):
         kvx.kvx_auto_path([1 << 30], [1 << 40], [8], None, "h2d", 7)
+
+
+def _run_with_env(code, **env_vars):
+    env = dict(os.environ, **env_vars)
+    return subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+
+
+def test_kvx_table_file_overrides_rows(tmp_path):
+    table = tmp_path / "gb300.table"
+    table.write_text("# dir max_mean variant budget threads unroll stages policy\n"
+                     "h2d 8192 bulk 7 256 8 5 0\n"
+                     "h2d inf ldg 33 512 4 3 1\n")
+    code = ("from expert_host_block_gb300 import kvx\n"
+            "print(kvx.kvx_default_launch('h2d', 4096))\n"
+            "print(kvx.kvx_default_launch('h2d', 16384))\n"
+            "print(kvx.kvx_default_launch('d2h', 4096))\n")
+    out = _run_with_env(code, KVX_TABLE=str(table))
+    lines = out.stdout.strip().splitlines()
+    assert "'variant': 2, 'cta_budget': 7" in lines[0] and "'stages': 5" in lines[0], out.stderr
+    assert "'cta_budget': 33, 'threads': 512, 'unroll': 4" in lines[1]
+    assert "'variant': 1, 'cta_budget': 64" in lines[2]  # no d2h row in the file: built-in row
+
+
+@pytest.mark.parametrize("text", ["h2d 4096 tma 8 256 8 3 0\n", "h2d 4096 ldg 8 300 8 3 0\n",
+                                  "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n"])
+def test_kvx_table_malformed_is_an_error(tmp_path, text):
+    table = tmp_path / "bad.table"
+    table.write_text(text)
+    code = ("from expert_host_block_gb300 import kvx\n"
+            "try:\n"
+            "    kvx.kvx_copy_batch([8], [16], [8], None, 0, 0, None)\n"
+            "except kvx.KvxError as e:\n"
+            "    print(e.status, e)\n")
+    out = _run_with_env(code, KVX_TABLE=str(table))
+    assert out.stdout.startswith(f"{kvx.KVX_ERR_INVALID_ARG} ") and "KVX_TABLE" in out.stdout, out.stdout + out.stderr
+    out = _run_with_env(code, KVX_TABLE=str(tmp_path / "missing.table"))
+    assert "cannot open" in out.stdout
+
+
+def test_kvx_log_reports_failures_on_stderr():
+    code = ("from expert_host_block_gb300 import kvx\n"
+            "print(kvx.kvx_validate([8], [16], [12], None, 0, 0))\n")
+    out = _run_with_env(code, KVX_LOG="1")
+    assert out.stdout.strip() == str(kvx.KVX_ERR_ALIGN)
+    assert "kvx: status 2:" in out.stderr and "multiples of 8" in out.stderr
+    out = _run_with_env(code, KVX_LOG="0")
+    assert "kvx:" not in out.stderr
+    bad = ("from expert_host_block_gb300 import kvx\n"
+           "try:\n"
+           "    kvx.kvx_copy_batch([8], [16], [8], None, 0, 0, None)\n"
+           "except kvx.KvxError as e:\n"
+           "    print(e.status, e)\n")
+    out = _run_with_env(bad, KVX_LOG="9")
+    assert out.stdout.startswith(f"{kvx.KVX_ERR_INVALID_ARG} ") and "KVX_LOG" in out.stdout
