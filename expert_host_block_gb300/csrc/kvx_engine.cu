@@ -167,6 +167,13 @@ const EnvSettings &env()
             else
                 e.error = std::string("KVX_LOG=") + v + " is not 0, 1 or 2";
         }
+        if (const char *v = getenv("KVX_PACK_THREADS")) {  // read by the worker pool
+            char *end = nullptr;
+            errno = 0;
+            long t = strtol(v, &end, 10);
+            if (errno || end == v || *end || t < 0 || t > 64)
+                e.error = std::string("KVX_PACK_THREADS=") + v + " is not an integer in [0, 64]";
+        }
         if (const char *v = getenv("KVX_TABLE")) {
             std::string err = parse_table(v, &e.table);
             if (!err.empty())
@@ -1127,6 +1134,26 @@ kvx_status kvx_stream_check(void *stream_)
                     (bits & kvx::kDevErrBadRecord) ? " chunk record longer than KVX_CHUNK_BYTES;" : "",
                     (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
                     (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
+    return KVX_OK;
+}
+
+kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_t *free_bytes,
+                            size_t *total_bytes)
+{
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    if (sm_count)
+        KVX_CUDA_TRY(cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev));
+    if (stack_bytes_per_thread)
+        KVX_CUDA_TRY(cudaDeviceGetLimit(stack_bytes_per_thread, cudaLimitStackSize));
+    if (free_bytes || total_bytes) {
+        size_t f = 0, t = 0;
+        KVX_CUDA_TRY(cudaMemGetInfo(&f, &t));
+        if (free_bytes)
+            *free_bytes = f;
+        if (total_bytes)
+            *total_bytes = t;
+    }
     return KVX_OK;
 }
 

@@ -55,7 +55,7 @@ EXPORTS = (
     "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
     "kvx_transfer_create", "kvx_transfer_start", "kvx_transfer_poll", "kvx_transfer_progress",
-    "kvx_transfer_destroy", "kvx_auto_path", "kvx_copy_batch_auto",
+    "kvx_transfer_destroy", "kvx_auto_path", "kvx_copy_batch_auto", "kvx_device_query",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
@@ -122,6 +122,8 @@ def _load():
         "kvx_transfer_progress": ([_vp, ctypes.POINTER(_sz), ctypes.POINTER(_sz)], _int),
         "kvx_transfer_destroy": ([_vp], _int),
         "kvx_auto_path": ([_vp, _vp, _vp, _sz, _int, _int, ctypes.POINTER(_int)], _int),
+        "kvx_device_query": ([ctypes.POINTER(_int), ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
+                             _int),
         "kvx_copy_batch_auto": ([_vp, _vp, _vp, _sz, _int, _int, _vp, ctypes.POINTER(_int)], _int),
         "kvx_devlist_destroy": ([_vp], _int),
         "kvx_copy_device_list": ([_vp, _u64, _u64, _u64, _u64, _int, ctypes.POINTER(kvx_launch), _vp], _int),
@@ -473,6 +475,14 @@ def kvx_version() -> int:
 
 def kvx_stream_check(stream=None) -> None:
     _check(_load().kvx_stream_check(_stream(stream)))
+
+
+def kvx_device_query() -> dict:
+    """SM count, per-thread stack limit and free / total memory of the current device."""
+    sms, stack, free, total = _int(), _sz(), _sz(), _sz()
+    _check(_load().kvx_device_query(ctypes.byref(sms), ctypes.byref(stack), ctypes.byref(free), ctypes.byref(total)))
+    return {"sm_count": sms.value, "stack_bytes_per_thread": stack.value, "free_bytes": free.value,
+            "total_bytes": total.value}
 
 
 def kvx_host_alloc(nbytes: int) -> int:

@@ -302,6 +302,16 @@ int kvx_version(void); /* KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR */
  * KVX_ERR_CUDA. */
 kvx_status kvx_stream_check(void *stream);
 
+/* The current device's SM count, per-thread stack limit and free / total
+ * memory (any pointer may be NULL): the inputs of a per-device launch profile,
+ * and the check against the sm_120 bulk-copy pitfall, where the
+ * .shared::cluster destination form made the driver raise the per-thread
+ * stack limit and hold 1.37 GiB of device memory (FreeToken issue #751,
+ * §What we changed). kvx uses the .shared::cta form, which leaves both
+ * unchanged. */
+kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_t *free_bytes,
+                            size_t *total_bytes);
+
 /* Mapped, portable pinned host memory (cudaHostAlloc). Fails with
  * KVX_ERR_NOT_MAPPED if the device address differs from the host address
  * (no unified addressing). Synchronous; not for the hot path. */
