@@ -625,13 +625,28 @@ void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
 }
 
 // mapped pinned words for kvx_stream_check
+constexpr unsigned kStatusWords = 1024;
 struct StatusWords {
     std::mutex mu;
-    unsigned *words = nullptr;
+    unsigned *words = nullptr;  // mapped pinned, written by the fetch kernel
+    cudaEvent_t events[kStatusWords] = {};
+    uint64_t gen[kStatusWords] = {};
     unsigned next = 0;
 };
 StatusWords g_status_words[kMaxDevices];
-constexpr unsigned kStatusWords = 1024;
+
+// The status a word of status bits stands for (kvx_stream_check's answer).
+kvx_status bits_status(unsigned bits)
+{
+    if (bits & kvx::kDevErrTimeout)
+        return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
+    if (bits)
+        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s", bits,
+                    (bits & kvx::kDevErrBadRecord) ? " chunk record longer than KVX_CHUNK_BYTES;" : "",
+                    (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
+                    (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
+    return KVX_OK;
+}
 
 // The common case of kvx_copy_batch_ex in one pass over the descriptors:
 // level-0 validation fused with packing into the staging slot. Sets *done and
@@ -1106,35 +1121,85 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     return KVX_OK;
 }
 
-kvx_status kvx_stream_check(void *stream_)
+kvx_status kvx_status_enqueue(void *stream_, kvx_status_token *tok)
 {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!tok)
+        return fail(KVX_ERR_INVALID_ARG, "null token");
     int dev = 0;
     KVX_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices)
         return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
     StatusWords &w = g_status_words[dev];
-    unsigned *word = nullptr;
-    {
-        std::lock_guard<std::mutex> g(w.mu);
-        if (!w.words)
-            KVX_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void **>(&w.words),
-                                       kStatusWords * sizeof(unsigned),
-                                       cudaHostAllocMapped | cudaHostAllocPortable));
-        word = w.words + (w.next++ % kStatusWords);
-    }
-    *word = 0;
-    KVX_CUDA_TRY(kvx::launch_status_fetch(word, stream));
-    KVX_CUDA_TRY(cudaStreamSynchronize(stream));
-    const unsigned bits = *reinterpret_cast<volatile unsigned *>(word);
-    if (bits & kvx::kDevErrTimeout)
-        return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
-    if (bits)
-        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s", bits,
-                    (bits & kvx::kDevErrBadRecord) ? " chunk record longer than KVX_CHUNK_BYTES;" : "",
-                    (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
-                    (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
+    std::lock_guard<std::mutex> g(w.mu);
+    if (!w.words)
+        KVX_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void **>(&w.words), kStatusWords * sizeof(unsigned),
+                                   cudaHostAllocMapped | cudaHostAllocPortable));
+    const unsigned slot = w.next++ % kStatusWords;
+    if (!w.events[slot])
+        KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.events[slot], cudaEventDisableTiming));
+    w.words[slot] = 0;
+    KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, stream));
+    KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
+    tok->slot = slot;
+    tok->gen = ++w.gen[slot];
+    tok->device = dev;
     return KVX_OK;
+}
+
+namespace {
+
+kvx_status token_slot(const kvx_status_token *tok, StatusWords **w)
+{
+    if (!tok || tok->device < 0 || tok->device >= kMaxDevices || tok->slot >= kStatusWords)
+        return fail(KVX_ERR_INVALID_ARG, "not a status token");
+    StatusWords &sw = g_status_words[tok->device];
+    std::lock_guard<std::mutex> g(sw.mu);
+    if (!sw.words || sw.gen[tok->slot] != tok->gen)
+        return fail(KVX_ERR_INVALID_ARG, "status token expired: %u later reads reused its slot", kStatusWords);
+    *w = &sw;
+    return KVX_OK;
+}
+
+}  // namespace
+
+kvx_status kvx_status_query(const kvx_status_token *tok, int *ready)
+{
+    if (!ready)
+        return fail(KVX_ERR_INVALID_ARG, "null output");
+    *ready = 0;
+    StatusWords *w = nullptr;
+    kvx_status st = token_slot(tok, &w);
+    if (st != KVX_OK)
+        return st;
+    const cudaError_t e = cudaEventQuery(w->events[tok->slot]);
+    if (e == cudaErrorNotReady) {
+        cudaGetLastError();
+        return KVX_OK;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaEventQuery(status read)");
+    *ready = 1;
+    return bits_status(*reinterpret_cast<volatile unsigned *>(w->words + tok->slot));
+}
+
+kvx_status kvx_status_wait(const kvx_status_token *tok)
+{
+    StatusWords *w = nullptr;
+    kvx_status st = token_slot(tok, &w);
+    if (st != KVX_OK)
+        return st;
+    KVX_CUDA_TRY(cudaEventSynchronize(w->events[tok->slot]));
+    return bits_status(*reinterpret_cast<volatile unsigned *>(w->words + tok->slot));
+}
+
+kvx_status kvx_stream_check(void *stream)
+{
+    kvx_status_token tok;
+    kvx_status st = kvx_status_enqueue(stream, &tok);
+    if (st != KVX_OK)
+        return st;
+    return kvx_status_wait(&tok);
 }
 
 kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_t *free_bytes,

@@ -56,9 +56,14 @@ EXPORTS = (
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
     "kvx_transfer_create", "kvx_transfer_start", "kvx_transfer_poll", "kvx_transfer_progress",
     "kvx_transfer_destroy", "kvx_auto_path", "kvx_copy_batch_auto", "kvx_device_query",
+    "kvx_status_enqueue", "kvx_status_wait", "kvx_status_query",
     # include/kvx_standin.h
     "kvx_standin_gemv_bf16",
 )
+
+
+class kvx_status_token(ctypes.Structure):
+    _fields_ = [("slot", ctypes.c_uint64), ("gen", ctypes.c_uint64), ("device", ctypes.c_int)]
 
 
 class kvx_launch(ctypes.Structure):
@@ -124,6 +129,9 @@ def _load():
         "kvx_auto_path": ([_vp, _vp, _vp, _sz, _int, _int, ctypes.POINTER(_int)], _int),
         "kvx_device_query": ([ctypes.POINTER(_int), ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)],
                              _int),
+        "kvx_status_enqueue": ([_vp, ctypes.POINTER(kvx_status_token)], _int),
+        "kvx_status_wait": ([ctypes.POINTER(kvx_status_token)], _int),
+        "kvx_status_query": ([ctypes.POINTER(kvx_status_token), ctypes.POINTER(_int)], _int),
         "kvx_copy_batch_auto": ([_vp, _vp, _vp, _sz, _int, _int, _vp, ctypes.POINTER(_int)], _int),
         "kvx_devlist_destroy": ([_vp], _int),
         "kvx_copy_device_list": ([_vp, _u64, _u64, _u64, _u64, _int, ctypes.POINTER(kvx_launch), _vp], _int),
@@ -475,6 +483,25 @@ def kvx_version() -> int:
 
 def kvx_stream_check(stream=None) -> None:
     _check(_load().kvx_stream_check(_stream(stream)))
+
+
+def kvx_status_enqueue(stream=None) -> kvx_status_token:
+    """Queue a read of the device status word behind the work on `stream`; returns its token."""
+    tok = kvx_status_token()
+    _check(_load().kvx_status_enqueue(_stream(stream), ctypes.byref(tok)))
+    return tok
+
+
+def kvx_status_wait(tok: kvx_status_token) -> None:
+    """Block until the read ran; raises like kvx_stream_check."""
+    _check(_load().kvx_status_wait(ctypes.byref(tok)))
+
+
+def kvx_status_query(tok: kvx_status_token) -> bool:
+    """True once the read ran (raising if it found an error); False while pending."""
+    r = _int()
+    _check(_load().kvx_status_query(ctypes.byref(tok), ctypes.byref(r)))
+    return bool(r.value)
 
 
 def kvx_device_query() -> dict:

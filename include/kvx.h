@@ -312,6 +312,26 @@ kvx_status kvx_stream_check(void *stream);
 kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_t *free_bytes,
                             size_t *total_bytes);
 
+/* The same read without blocking, for a transfer worker that submits the
+ * next batch before collecting the previous one (the enqueue-only contract of
+ * PegaFlow issue #408, follow-up §2: record completion, poll it later).
+ * kvx_status_enqueue queues a read of the status word behind the work already
+ * on `stream` and returns a token; kvx_status_wait blocks until that read has
+ * run and returns what kvx_stream_check would have; kvx_status_query does not
+ * block (*ready = 0 while the stream has not reached the read; otherwise
+ * *ready = 1 and the status). Reading clears the word, and the word is shared
+ * by all streams of the device. A token stays valid for the next 1,024 reads
+ * enqueued on its device; after that, KVX_ERR_INVALID_ARG. */
+typedef struct kvx_status_token {
+    uint64_t slot; /* opaque */
+    uint64_t gen;  /* opaque */
+    int device;
+} kvx_status_token;
+
+kvx_status kvx_status_enqueue(void *stream, kvx_status_token *tok);
+kvx_status kvx_status_wait(const kvx_status_token *tok);
+kvx_status kvx_status_query(const kvx_status_token *tok, int *ready);
+
 /* Mapped, portable pinned host memory (cudaHostAlloc). Fails with
  * KVX_ERR_NOT_MAPPED if the device address differs from the host address
  * (no unified addressing). Synchronous; not for the hot path. */

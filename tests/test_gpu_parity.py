@@ -511,3 +511,42 @@ def test_bulk_ring_sizes_with_mixed_alignment(stages, size_kib):
         _one(p, b, launch={"variant": "bulk", "cta_budget": 5, "stages": stages})
     finally:
         p.close()
+
+
+def test_status_tokens_pipelined():
+    """Submit, enqueue a status read, submit more, then collect: the enqueue-only pattern."""
+    w = W.kv_burst(n_sets=4, n_per_dir=2048, pool_bytes=64 * W.MIB)
+    p = Pools(w.pools)
+    try:
+        want = p.expected([b for pair in w.batches for b in pair])
+        s1 = torch.cuda.Stream()
+        toks = []
+        for h2d, d2h in w.batches:
+            run_batch(p, h2d, stream=s1)
+            run_batch(p, d2h, stream=s1)
+            toks.append(kvx.kvx_status_enqueue(s1))
+        for t in toks:
+            kvx.kvx_status_wait(t)
+            assert kvx.kvx_status_query(t) is True
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+def test_status_token_pending_then_timeout_then_expiry():
+    s = torch.cuda.Stream()
+    kvx.kvx_stream_check(s)
+    kvx.kvx_selftest_wait_timeout(200_000_000, s)  # 200 ms of GPU work that ends in a timeout bit
+    tok = kvx.kvx_status_enqueue(s)
+    assert kvx.kvx_status_query(tok) is False  # the stream has not reached the read yet
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_status_wait(tok)
+    assert e.value.status == kvx.KVX_ERR_TIMEOUT
+    old = kvx.kvx_status_enqueue(s)
+    kvx.kvx_status_wait(old)
+    for _ in range(1024):
+        kvx.kvx_status_enqueue(s)
+    torch.cuda.synchronize()
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_status_wait(old)
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
