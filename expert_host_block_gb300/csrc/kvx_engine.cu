@@ -525,6 +525,7 @@ struct Slot {
     kvx_chunk *dev = nullptr;
     size_t cap = 0;             // chunks
     cudaEvent_t done = nullptr;
+    cudaEvent_t uploaded = nullptr;  // recorded after a side-stream upload of the table
     bool recorded = false;
     bool busy = false;          // held by a caller between acquire and release
     uint64_t stamp = 0;         // release order: larger = more recently packed
@@ -615,6 +616,64 @@ kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
     return KVX_OK;
 }
 
+// Side streams of each device: one for chunk-table uploads, one for status
+// reads. Created on first use with the device's highest priority, never
+// destroyed.
+enum AuxKind { kAuxUpload = 0, kAuxStatus = 1, kAuxKinds = 2 };
+struct AuxStreams {
+    std::mutex mu;
+    cudaStream_t s[kAuxKinds] = {};
+};
+AuxStreams g_aux[kMaxDevices];
+
+cudaError_t aux_stream(int dev, AuxKind kind, cudaStream_t *out)
+{
+    AuxStreams &a = g_aux[dev];
+    std::lock_guard<std::mutex> g(a.mu);
+    if (!a.s[kind]) {
+        int least = 0, greatest = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaStreamCreateWithPriority(&a.s[kind], cudaStreamNonBlocking, greatest);
+        if (e != cudaSuccess) {
+            a.s[kind] = nullptr;
+            return e;
+        }
+    }
+    *out = a.s[kind];
+    return cudaSuccess;
+}
+
+// Upload a packed chunk table from its pinned slot to the slot's device table,
+// ordered before whatever is enqueued on `stream` next. ring_acquire returned
+// the slot only after the last kernel reading its device table finished, so
+// the upload depends on nothing already on `stream`. When `stream` is idle it
+// goes on `stream`; when work is still queued there (a transfer worker that
+// submits the next burst while the previous one copies) it goes on the upload
+// side stream and `stream` waits for it, so the upload overlaps that work
+// instead of idling the link between two copy kernels.
+cudaError_t upload_table(int dev, Slot *s, size_t bytes, cudaStream_t stream)
+{
+    cudaError_t q = cudaStreamQuery(stream);
+    if (q == cudaSuccess)
+        return cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, stream);
+    if (q != cudaErrorNotReady)
+        return q;
+    cudaGetLastError();  // cudaErrorNotReady is not sticky; clear it
+    cudaStream_t side = nullptr;
+    cudaError_t e = aux_stream(dev, kAuxUpload, &side);
+    if (e == cudaSuccess && !s->uploaded)
+        e = cudaEventCreateWithFlags(&s->uploaded, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, side);
+    if (e == cudaSuccess)
+        e = cudaEventRecord(s->uploaded, side);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(stream, s->uploaded, 0);
+    return e;
+}
+
 void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
 {
     if (record && cudaEventRecord(s->done, stream) == cudaSuccess)
@@ -629,7 +688,8 @@ constexpr unsigned kStatusWords = 1024;
 struct StatusWords {
     std::mutex mu;
     unsigned *words = nullptr;  // mapped pinned, written by the fetch kernel
-    cudaEvent_t events[kStatusWords] = {};
+    cudaEvent_t marks[kStatusWords] = {};   // the caller's stream reached the read
+    cudaEvent_t events[kStatusWords] = {};  // the read has run
     uint64_t gen[kStatusWords] = {};
     unsigned next = 0;
 };
@@ -682,11 +742,10 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     }
     *done = true;
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
-    cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
-                                    cudaMemcpyHostToDevice, stream);
+    cudaError_t e = upload_table(dev, s, (size_t)chunks * sizeof(kvx_chunk), stream);
     if (e != cudaSuccess) {
         ring_release(dev, s, stream, false);
-        return cuda_fail(e, "cudaMemcpyAsync(chunk table)");
+        return cuda_fail(e, "chunk table upload");
     }
     e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, max_chunk, stream);
     ring_release(dev, s, stream, true);
@@ -840,11 +899,10 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
         return st;
     pack(src, dst, sizes, n, s->host);
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
-    cudaError_t e = cudaMemcpyAsync(s->dev, s->host, (size_t)chunks * sizeof(kvx_chunk),
-                                    cudaMemcpyHostToDevice, stream);
+    cudaError_t e = upload_table(dev, s, (size_t)chunks * sizeof(kvx_chunk), stream);
     if (e != cudaSuccess) {
         ring_release(dev, s, stream, false);
-        return cuda_fail(e, "cudaMemcpyAsync(chunk table)");
+        return cuda_fail(e, "chunk table upload");
     }
     e = kvx::launch_copy(l, s->dev, (uint32_t)chunks, max_chunk, stream);
     ring_release(dev, s, stream, true);
@@ -1135,12 +1193,30 @@ kvx_status kvx_status_enqueue(void *stream_, kvx_status_token *tok)
     if (!w.words)
         KVX_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void **>(&w.words), kStatusWords * sizeof(unsigned),
                                    cudaHostAllocMapped | cudaHostAllocPortable));
+    bool cap = false;
+    kvx_status st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
     const unsigned slot = w.next++ % kStatusWords;
     if (!w.events[slot])
         KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.events[slot], cudaEventDisableTiming));
+    if (!w.marks[slot])
+        KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.marks[slot], cudaEventDisableTiming));
     w.words[slot] = 0;
-    KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, stream));
-    KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
+    if (cap) {
+        // inside a capture the read becomes a node of the graph
+        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, stream));
+        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
+    } else {
+        // the read waits for the work already on `stream`, on a side stream,
+        // so that the next copy on `stream` does not wait for the read
+        cudaStream_t side = nullptr;
+        KVX_CUDA_TRY(aux_stream(dev, kAuxStatus, &side));
+        KVX_CUDA_TRY(cudaEventRecord(w.marks[slot], stream));
+        KVX_CUDA_TRY(cudaStreamWaitEvent(side, w.marks[slot], 0));
+        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, side));
+        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], side));
+    }
     tok->slot = slot;
     tok->gen = ++w.gen[slot];
     tok->device = dev;

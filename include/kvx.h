@@ -130,7 +130,10 @@ typedef struct kvx_desc_buf kvx_desc_buf;
  * ring has 8 slots per device; a call takes the most recently used slot whose
  * copy has finished, and waits on the host only when none has (then for the
  * least recently used one). A slot allocates on first use and grows, once, for
- * a batch bigger than it holds. */
+ * a batch bigger than it holds. When `stream` still has work queued, the
+ * table upload runs on a library side stream (overlapping that work) and the
+ * copy kernel waits for it on `stream`; the copy stays ordered after all
+ * earlier work on `stream` either way. */
 kvx_status kvx_copy_batch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                           const uint64_t *sizes, size_t n, int dir, int cta_budget,
                           void *stream);
@@ -320,7 +323,11 @@ kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_
  * run and returns what kvx_stream_check would have; kvx_status_query does not
  * block (*ready = 0 while the stream has not reached the read; otherwise
  * *ready = 1 and the status). Reading clears the word, and the word is shared
- * by all streams of the device. A token stays valid for the next 1,024 reads
+ * by all streams of the device. Outside a graph capture the read runs on a
+ * library side stream once `stream` reaches it, so work enqueued on `stream`
+ * after the token does not wait for the read (and an error that such work
+ * raises may be reported by this token rather than the next). Inside a capture
+ * the read is a node on `stream`. A token stays valid for the next 1,024 reads
  * enqueued on its device; after that, KVX_ERR_INVALID_ARG. */
 typedef struct kvx_status_token {
     uint64_t slot; /* opaque */
