@@ -89,9 +89,10 @@ struct EnvSettings {
 };
 
 // A launch table in a text file: one row per line, `#` starts a comment:
-//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy
+//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy [assign]
 // with dir h2d|d2h|d2d, max_mean_chunk_bytes an integer or "inf", variant
-// ldg|bulk. Rows are tried in file order, before the built-in rows.
+// ldg|bulk, assign static|dynamic (absent: the built-in choice for dir).
+// Rows are tried in file order, before the built-in rows.
 std::string parse_table(const char *path, std::vector<TableRow> *rows)
 {
     FILE *f = fopen(path, "r");
@@ -104,10 +105,10 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         ++lineno;
         if (char *h = strchr(line, '#'))
             *h = 0;
-        char dir[16], maxs[32], var[16];
+        char dir[16], maxs[32], var[16], asg[16] = "";
         int budget, threads, unroll, stages, policy;
-        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d", dir, maxs, var, &budget, &threads,
-                               &unroll, &stages, &policy);
+        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s", dir, maxs, var, &budget, &threads,
+                               &unroll, &stages, &policy, asg);
         if (got <= 0)
             continue;  // blank or comment
         TableRow r{};
@@ -118,14 +119,17 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         else
             r.max_mean_chunk = strtoull(maxs, &end, 10);
         const int variant = !strcmp(var, "ldg") ? KVX_VARIANT_LDG : !strcmp(var, "bulk") ? KVX_VARIANT_BULK : -1;
-        if (got != 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
+        const int assign = got < 9 ? KVX_ASSIGN_AUTO
+                           : !strcmp(asg, "static") ? KVX_ASSIGN_STATIC
+                           : !strcmp(asg, "dynamic") ? KVX_ASSIGN_DYNAMIC : -1;
+        if (got < 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
             (threads != 128 && threads != 256 && threads != 512) || (unroll != 2 && unroll != 4 && unroll != 8) ||
-            stages < 2 || stages > 12 || policy < 0 || policy > 2) {
+            stages < 2 || stages > 12 || policy < 0 || policy > 2 || assign < 0) {
             err = std::string("KVX_TABLE=") + path + ": line " + std::to_string(lineno) +
-                  " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy'";
+                  " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy [assign]'";
             break;
         }
-        r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy};
+        r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy, assign};
         rows->push_back(r);
     }
     fclose(f);
@@ -442,18 +446,31 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // chunks averaging 12 KiB or more, the bulk ring measured faster (3.28-3.36
 // TB/s of payload with 608 one-warp CTAs and 96 KiB rings, against 3.24 for
 // LDG), so that size class picks it.
+//
+// Work assignment: over the host link the LDG warps take units from a counter
+// (joined KV bursts 329 against 324 GB/s by position; single-direction cells
+// unchanged or up to 1.5 % faster). D2D keeps the assignment by position: its
+// units take ~1 us, so one counter shared by 2,432 warps contends (4 KiB x
+// 65,536 chunks: 2.1 against 3.2 TB/s).
 const TableRow kTable[] = {
-    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
-    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0}},
-    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 608, 256, 8, 6, 0}},
+    {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
+    {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
+    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 608, 256, 8, 6, 0, KVX_ASSIGN_STATIC}},
 };
+
+int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
 
 kvx_launch table_launch(int dir, uint64_t mean_chunk)
 {
-    for (const TableRow &r : env().table)  // KVX_TABLE rows first
-        if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
-            return r.cfg;
+    for (const TableRow &r : env().table) {  // KVX_TABLE rows first
+        if (r.dir == dir && mean_chunk <= r.max_mean_chunk) {
+            kvx_launch c = r.cfg;
+            if (c.assign == KVX_ASSIGN_AUTO)
+                c.assign = default_assign(dir);
+            return c;
+        }
+    }
     for (const TableRow &r : kTable)
         if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
             return r.cfg;
@@ -471,6 +488,7 @@ kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch 
     int unroll = (want && want->unroll) ? want->unroll : t.unroll;
     int stages = (want && want->stages) ? want->stages : t.stages;
     int policy = (want && want->store_policy) ? want->store_policy : t.store_policy;
+    int assign = (want && want->assign) ? want->assign : t.assign;
     if (want) {
         if (want->variant < 0 || want->variant > KVX_VARIANT_BULK)
             return fail(KVX_ERR_INVALID_ARG, "variant %d is not AUTO, LDG or BULK", want->variant);
@@ -484,6 +502,8 @@ kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch 
             return fail(KVX_ERR_INVALID_ARG, "stages %d is not in 2..12", want->stages);
         if (want->store_policy < 0 || want->store_policy > 2)
             return fail(KVX_ERR_INVALID_ARG, "store_policy %d is not 0, 1 or 2", want->store_policy);
+        if (want->assign < 0 || want->assign > KVX_ASSIGN_DYNAMIC)
+            return fail(KVX_ERR_INVALID_ARG, "assign %d is not AUTO, STATIC or DYNAMIC", want->assign);
     }
     if (variant == KVX_VARIANT_AUTO)
         variant = t.variant;
@@ -493,6 +513,7 @@ kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch 
     out->unroll = unroll;
     out->stages = stages;
     out->store_policy = policy;
+    out->assign = assign;
     return KVX_OK;
 }
 
@@ -500,9 +521,9 @@ void log_batch(const char *entry, int dir, size_t n, uint64_t chunks, uint64_t b
 {
     if (log_level() >= 2)
         fprintf(stderr, "kvx: %s dir=%d n=%zu chunks=%llu bytes=%llu variant=%d ctas=%d threads=%d unroll=%d "
-                        "stages=%d\n",
+                        "stages=%d assign=%d\n",
                 entry, dir, n, (unsigned long long)chunks, (unsigned long long)bytes, l.variant, l.ctas,
-                l.threads, l.unroll, l.stages);
+                l.threads, l.unroll, l.stages, l.assign);
 }
 
 kvx_status is_capturing(cudaStream_t stream, bool *cap)
@@ -521,9 +542,9 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kMinSlotChunks = 1 << 16;
 
 struct Slot {
-    kvx_chunk *host = nullptr;  // pinned
-    kvx_chunk *dev = nullptr;
-    size_t cap = 0;             // chunks
+    kvx_chunk *host = nullptr;  // pinned: the table header (kept zero), then the records
+    kvx_chunk *dev = nullptr;   // the device table: header, then records
+    size_t cap = 0;             // chunks (records after the header)
     cudaEvent_t done = nullptr;
     cudaEvent_t uploaded = nullptr;  // recorded after a side-stream upload of the table
     bool recorded = false;
@@ -600,11 +621,12 @@ kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
         s->host = nullptr;
         s->dev = nullptr;
         s->cap = 0;
-        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&s->host), cap * sizeof(kvx_chunk),
-                                      cudaHostAllocPortable);
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&s->host),
+                                      (cap + kvx::kTableHeader) * sizeof(kvx_chunk), cudaHostAllocPortable);
         if (e != cudaSuccess)
             return release_on_error(cuda_fail(e, "cudaHostAlloc(staging slot)"));
-        e = cudaMalloc(reinterpret_cast<void **>(&s->dev), cap * sizeof(kvx_chunk));
+        memset(s->host, 0, kvx::kTableHeader * sizeof(kvx_chunk));
+        e = cudaMalloc(reinterpret_cast<void **>(&s->dev), (cap + kvx::kTableHeader) * sizeof(kvx_chunk));
         if (e != cudaSuccess) {
             cudaFreeHost(s->host);
             s->host = nullptr;
@@ -735,14 +757,15 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     uint64_t chunks = 0, payload = 0;
     uint32_t max_chunk = 0;
     Launch l;
-    if (!pack_fast(src, dst, sizes, n, s->host, &chunks, &payload, &max_chunk) || payload == 0 ||
+    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk) ||
+        payload == 0 ||
         resolve(dir, payload / chunks, want, &l) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;
     }
     *done = true;
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
-    cudaError_t e = upload_table(dev, s, (size_t)chunks * sizeof(kvx_chunk), stream);
+    cudaError_t e = upload_table(dev, s, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk), stream);
     if (e != cudaSuccess) {
         ring_release(dev, s, stream, false);
         return cuda_fail(e, "chunk table upload");
@@ -768,10 +791,11 @@ struct kvx_desc_buf {
     std::mutex mu;
     int device = 0;
     size_t cap = 0;
-    kvx_chunk *dev = nullptr;
-    kvx_chunk *host = nullptr;
+    kvx_chunk *dev = nullptr;   // header record, then the chunk records
+    kvx_chunk *host = nullptr;  // pinned staging, same layout (header kept zero)
     cudaEvent_t upload_done = nullptr;
     cudaEvent_t last_use = nullptr;
+    cudaStream_t last_stream = nullptr;  // stream of the last copy
     bool upload_recorded = false;
     bool use_recorded = false;
     uint32_t n_chunks = 0;
@@ -897,9 +921,9 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     st = ring_acquire(dev, (size_t)chunks, &s);
     if (st != KVX_OK)
         return st;
-    pack(src, dst, sizes, n, s->host);
+    pack(src, dst, sizes, n, s->host + kvx::kTableHeader);
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
-    cudaError_t e = upload_table(dev, s, (size_t)chunks * sizeof(kvx_chunk), stream);
+    cudaError_t e = upload_table(dev, s, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk), stream);
     if (e != cudaSuccess) {
         ring_release(dev, s, stream, false);
         return cuda_fail(e, "chunk table upload");
@@ -932,11 +956,13 @@ kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
     if (!b)
         return fail(KVX_ERR_CAPACITY, "out of host memory");
     cudaError_t e = cudaGetDevice(&b->device);
+    const size_t bytes = (max_chunks + kvx::kTableHeader) * sizeof(kvx_chunk);
     if (e == cudaSuccess)
-        e = cudaMalloc(reinterpret_cast<void **>(&b->dev), max_chunks * sizeof(kvx_chunk));
+        e = cudaMalloc(reinterpret_cast<void **>(&b->dev), bytes);
     if (e == cudaSuccess)
-        e = cudaHostAlloc(reinterpret_cast<void **>(&b->host), max_chunks * sizeof(kvx_chunk),
-                          cudaHostAllocPortable);
+        e = cudaHostAlloc(reinterpret_cast<void **>(&b->host), bytes, cudaHostAllocPortable);
+    if (e == cudaSuccess)
+        memset(b->host, 0, kvx::kTableHeader * sizeof(kvx_chunk));
     if (e == cudaSuccess)
         e = cudaEventCreateWithFlags(&b->upload_done, cudaEventDisableTiming);
     if (e == cudaSuccess)
@@ -988,9 +1014,9 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
         KVX_CUDA_TRY(cudaEventSynchronize(b->upload_done));
         b->upload_recorded = false;
     }
-    pack(src, dst, sizes, n, b->host);
+    pack(src, dst, sizes, n, b->host + kvx::kTableHeader);
     if (chunks)
-        KVX_CUDA_TRY(cudaMemcpyAsync(b->dev, b->host, (size_t)chunks * sizeof(kvx_chunk),
+        KVX_CUDA_TRY(cudaMemcpyAsync(b->dev, b->host, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                      cudaMemcpyHostToDevice, stream));
     KVX_CUDA_TRY(cudaEventRecord(b->upload_done, stream));
     b->upload_recorded = true;
@@ -998,7 +1024,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     b->max_chunk = max_chunk;
     b->payload = payload;
     b->dir = dir;
-    b->selected = {l.variant, l.ctas, l.threads, l.unroll, l.stages, l.store_policy};
+    b->selected = {l.variant, l.ctas, l.threads, l.unroll, l.stages, l.store_policy, l.assign};
     return KVX_OK;
 }
 
@@ -1027,6 +1053,8 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
             merged.stages = want->stages;
         if (want->store_policy)
             merged.store_policy = want->store_policy;
+        if (want->assign)
+            merged.assign = want->assign;
     }
     Launch l;
     st = resolve(b->dir, 0, &merged, &l);
@@ -1038,12 +1066,17 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
+    // two copies over one table must not overlap: order this one after the
+    // buffer's previous copy when that ran on another stream
+    if (!cap && b->use_recorded && b->last_stream != stream)
+        KVX_CUDA_TRY(cudaStreamWaitEvent(stream, b->last_use, 0));
     cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     if (!cap) {
         KVX_CUDA_TRY(cudaEventRecord(b->last_use, stream));
         b->use_recorded = true;
+        b->last_stream = stream;
     }
     return KVX_OK;
 }
@@ -1393,14 +1426,15 @@ kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 // ---------------------------------------------------------------------------
 namespace {
 
-// The chunk table of kvx_copy_batch_noalloc, in the library's own device
-// memory: every GPU that loads the library holds these 2 MiB until exit.
-static __device__ __align__(256) kvx_chunk g_noalloc_table[KVX_NOALLOC_MAX_CHUNKS];
+// The chunk table of kvx_copy_batch_noalloc (its header record, then up to
+// KVX_NOALLOC_MAX_CHUNKS records), in the library's own device memory: every
+// GPU that loads the library holds these 2 MiB until exit.
+static __device__ __align__(256) kvx_chunk g_noalloc_table[kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS];
 
-// Host side of the table. It is packed here and copied with a pageable
-// cudaMemcpyAsync, which stages the bytes before it returns, so the array can
-// be refilled as soon as the call returns.
-kvx_chunk g_noalloc_stage[KVX_NOALLOC_MAX_CHUNKS];
+// Host side of the table, same layout, header kept zero. It is packed here and
+// copied with a pageable cudaMemcpyAsync, which stages the bytes before it
+// returns, so the array can be refilled as soon as the call returns.
+kvx_chunk g_noalloc_stage[kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS];
 
 // Serialises callers from pack to launch: the host array has one owner at a
 // time, and calls on one stream enqueue upload and kernel back to back.
@@ -1452,8 +1486,9 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
             return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk table)");
         g_noalloc_dev[dev] = static_cast<kvx_chunk *>(p);
     }
-    pack(src, dst, sizes, n, g_noalloc_stage);
-    KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage, (size_t)chunks * sizeof(kvx_chunk),
+    pack(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader);
+    KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage,
+                                 (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                  cudaMemcpyHostToDevice, stream));
     cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, max_chunk, stream);
     if (e != cudaSuccess)

@@ -37,15 +37,23 @@ struct Launch {
     int unroll;        // LDG 16-byte loads in flight per lane
     int stages;        // BULK ring size in units of KVX_CHUNK_BYTES
     int store_policy;  // LDG store cache policy
+    int assign;        // LDG: KVX_ASSIGN_STATIC or KVX_ASSIGN_DYNAMIC
 };
+
+// Every device chunk table starts with one header record that holds the
+// dynamic-assignment counters (next unit, warps done); the chunk records
+// follow it. The header is zero after every upload (the host staging copy
+// keeps it zero) and after every copy (the last warp zeroes it).
+constexpr size_t kTableHeader = 1;
 
 // Grid needed to give every CTA some work, for a chunk count, the longest
 // chunk and the variant.
 int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
 
-// Enqueue the copy kernel over a device-resident chunk table. max_chunk_len is
-// the longest record's len (it sets the LDG kernel's passes per chunk).
-cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
+// Enqueue the copy kernel over a device-resident chunk table: `table` points at
+// its header record, n_chunks records follow. max_chunk_len is the longest
+// record's len (it sets the LDG kernel's passes per chunk).
+cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
                         uint32_t max_chunk_len, cudaStream_t stream);
 
 // Enqueue the plan and copy kernels over a device-resident descriptor list:

@@ -255,37 +255,94 @@ __device__ __forceinline__ Rec shfl_rec(const Rec &r, int src_lane)
 
 // Work units are warp passes in pass-major order: unit u is pass
 // u / n_chunks of chunk u % n_chunks, for `passes` passes per chunk (enough for
-// the batch's longest chunk). Unit u goes to warp u mod (warps in the grid).
-// Whatever the mix of chunk lengths, no warp ends with more than one pass more
-// than another, and for a batch of chunks that fit one pass every unit is a
-// whole chunk. A warp reads the records of its next 32 units with one load
-// per lane and hands them around with shuffles.
+// the batch's longest chunk). For a batch of chunks that fit one pass every
+// unit is a whole chunk.
+//
+// Static assignment (ctr == nullptr): unit u goes to warp u mod (warps in the
+// grid). Whatever the mix of chunk lengths, no warp ends with more than one
+// pass more than another. A warp reads the records of its next 32 units with
+// one load per lane and hands them around with shuffles.
+//
+// Dynamic assignment (ctr != nullptr): warp w copies unit w first, then takes
+// one unit at a time from the counter ctr[0]. Over the host link the warps are
+// not served equally fast: by position, the first warps of a KV-burst launch
+// were done after 60 % of the launch and the last ones set its length. Taking
+// units from a counter, every warp stays busy to within about one unit of the
+// end. Lane 0 keeps the pipeline: while unit k is copied, the record of unit
+// k+1 and the index of unit k+2 are already on their way, so neither latency
+// adds to the copy. The last warp to finish (counted in ctr[1]) zeroes both
+// words for the next launch over the same table.
+__device__ __forceinline__ Rec unit_rec(const kvx_chunk *__restrict__ tab, uint64_t u, uint32_t n_chunks,
+                                        uint32_t pass_bytes, uint32_t *pass_out)
+{
+    const uint64_t pass = u / n_chunks;
+    Rec r = load_rec(tab, u - pass * n_chunks);
+    if (pass * pass_bytes >= r.l)
+        r.l = 0;  // this chunk has no such pass
+    *pass_out = (uint32_t)pass;
+    return r;
+}
+
 template <int U, int P>
 __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
-                                                            uint32_t n_chunks, uint32_t passes)
+                                                            uint32_t n_chunks, uint32_t passes,
+                                                            unsigned long long *ctr)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t wpb = blockDim.x >> 5;
     const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
     const uint64_t n_units = (uint64_t)n_chunks * passes;
-    for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
-        const uint64_t mine = base + (uint64_t)lane * nwarps;
-        Rec r = {0, 0, 0};
-        uint32_t k = 0;
-        if (mine < n_units) {
-            const uint64_t pass = mine / n_chunks;
-            k = (uint32_t)pass;
-            r = load_rec(tab, mine - pass * n_chunks);
-            if ((uint64_t)k * PassBytes<U>::value >= r.l)
-                r.l = 0;  // this chunk has no pass k
+    if (ctr == nullptr) {
+        for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
+            const uint64_t mine = base + (uint64_t)lane * nwarps;
+            Rec r = {0, 0, 0};
+            uint32_t k = 0;
+            if (mine < n_units)
+                r = unit_rec(tab, mine, n_chunks, PassBytes<U>::value, &k);
+            const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
+            for (int j = 0; j < cnt; ++j) {
+                const Rec c = shfl_rec(r, j);
+                const uint32_t kk = __shfl_sync(kFull, k, j);
+                if (c.l)
+                    copy_pass<U, P>(c.s, c.d, c.l, kk, lane);
+            }
         }
-        const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
-        for (int j = 0; j < cnt; ++j) {
-            const Rec c = shfl_rec(r, j);
-            const uint32_t kk = __shfl_sync(kFull, k, j);
-            if (c.l)
-                copy_pass<U, P>(c.s, c.d, c.l, kk, lane);
+        return;
+    }
+    // lane 0: rc / kc = record and pass of the current unit, nx = the next unit
+    uint64_t cur = gwarp;
+    unsigned long long nx = 0;
+    Rec rc = {0, 0, 0};
+    uint32_t kc = 0;
+    if (lane == 0) {
+        nx = nwarps + atomicAdd(&ctr[0], 1ull);
+        if (cur < n_units)
+            rc = unit_rec(tab, cur, n_chunks, PassBytes<U>::value, &kc);
+    }
+    while (cur < n_units) {
+        unsigned long long nn = 0;
+        Rec rn = {0, 0, 0};
+        uint32_t kn = 0;
+        if (lane == 0) {
+            nn = nwarps + atomicAdd(&ctr[0], 1ull);
+            if (nx < n_units)
+                rn = unit_rec(tab, nx, n_chunks, PassBytes<U>::value, &kn);
+        }
+        const Rec c = shfl_rec(rc, 0);
+        const uint32_t kk = __shfl_sync(kFull, kc, 0);
+        if (c.l)
+            copy_pass<U, P>(c.s, c.d, c.l, kk, lane);
+        cur = __shfl_sync(kFull, nx, 0);
+        nx = nn;
+        rc = rn;
+        kc = kn;
+    }
+    if (lane == 0) {
+        __threadfence();  // this warp's counter updates before its count of done warps
+        if (atomicAdd(&ctr[1], 1ull) == nwarps - 1) {
+            atomicExch(&ctr[0], 0ull);
+            atomicExch(&ctr[1], 0ull);
         }
     }
 }
@@ -710,20 +767,20 @@ __global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns)
 
 template <int U, int P>
 cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
-                       cudaStream_t s)
+                       unsigned long long *ctr, cudaStream_t s)
 {
-    kvx_copy_ldg_kernel<U, P><<<ctas, threads, 0, s>>>(t, n, passes);
+    kvx_copy_ldg_kernel<U, P><<<ctas, threads, 0, s>>>(t, n, passes, ctr);
     return cudaGetLastError();
 }
 
 template <int U>
 cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint32_t n,
-                         uint32_t passes, cudaStream_t s)
+                         uint32_t passes, unsigned long long *ctr, cudaStream_t s)
 {
     switch (p) {
-    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, s);
-    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, s);
-    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, s);
+    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, ctr, s);
+    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, ctr, s);
+    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, ctr, s);
     }
 }
 
@@ -783,20 +840,23 @@ int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
     return (int)((uint64_t)l.ctas < need ? (uint64_t)l.ctas : need);
 }
 
-cudaError_t launch_copy(const Launch &l, const kvx_chunk *table, uint32_t n_chunks,
+cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
                         uint32_t max_chunk_len, cudaStream_t stream)
 {
     if (n_chunks == 0)
         return cudaSuccess;
     const int ctas = work_ctas(l, n_chunks, max_chunk_len);
+    const kvx_chunk *recs = table + kTableHeader;
     if (l.variant == KVX_VARIANT_BULK) {
-        return launch_bulk(ctas, l.stages, table, n_chunks, max_chunk_len, stream);
+        return launch_bulk(ctas, l.stages, recs, n_chunks, max_chunk_len, stream);
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
+    unsigned long long *ctr =
+        l.assign == KVX_ASSIGN_DYNAMIC ? reinterpret_cast<unsigned long long *>(table) : nullptr;
     switch (l.unroll) {
-    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
-    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
-    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, table, n_chunks, passes, stream);
+    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, stream);
+    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, stream);
+    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, stream);
     }
 }
 

@@ -27,6 +27,8 @@ KVX_H2D, KVX_D2H, KVX_D2D = 0, 1, 2
 DIRS = {"h2d": KVX_H2D, "d2h": KVX_D2H, "d2d": KVX_D2D}
 KVX_VARIANT_AUTO, KVX_VARIANT_LDG, KVX_VARIANT_BULK = 0, 1, 2
 VARIANTS = {"auto": KVX_VARIANT_AUTO, "ldg": KVX_VARIANT_LDG, "bulk": KVX_VARIANT_BULK}
+KVX_ASSIGN_AUTO, KVX_ASSIGN_STATIC, KVX_ASSIGN_DYNAMIC = 0, 1, 2
+ASSIGNS = {"auto": KVX_ASSIGN_AUTO, "static": KVX_ASSIGN_STATIC, "dynamic": KVX_ASSIGN_DYNAMIC}
 
 KVX_OK = 0
 KVX_ERR_INVALID_ARG = 1
@@ -38,6 +40,9 @@ KVX_ERR_CUDA = 6
 KVX_ERR_TIMEOUT = 7
 KVX_ERR_DEVICE_FAULT = 8
 KVX_ERR_CAPTURE = 9
+
+# the C ABI version this binding's structures follow (KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR)
+KVX_VERSION = 2
 
 KVX_CHUNK_BYTES = 16384
 KVX_MAX_CHUNKS = 1 << 22
@@ -68,7 +73,8 @@ class kvx_status_token(ctypes.Structure):
 
 class kvx_launch(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("cta_budget", ctypes.c_int), ("threads", ctypes.c_int),
-                ("unroll", ctypes.c_int), ("stages", ctypes.c_int), ("store_policy", ctypes.c_int)]
+                ("unroll", ctypes.c_int), ("stages", ctypes.c_int), ("store_policy", ctypes.c_int),
+                ("assign", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -141,6 +147,9 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = res
+    if lib.kvx_version() != KVX_VERSION:
+        raise RuntimeError(f"{LIB_PATH} implements C ABI version {lib.kvx_version()}, this binding "
+                           f"version {KVX_VERSION}: rebuild the library")
     _lib = lib
     return lib
 
@@ -198,6 +207,8 @@ def _launch(launch) -> kvx_launch | None:
     v = dict(launch)
     if isinstance(v.get("variant"), str):
         v["variant"] = VARIANTS[v["variant"]]
+    if isinstance(v.get("assign"), str):
+        v["assign"] = ASSIGNS[v["assign"]]
     return kvx_launch(**v)
 
 

@@ -59,7 +59,7 @@ extern "C" {
 #endif
 
 #define KVX_VERSION_MAJOR 0
-#define KVX_VERSION_MINOR 1
+#define KVX_VERSION_MINOR 2
 
 /* Largest chunk a descriptor is cut into: 16 KiB, the chunk of the FreeToken
  * gather (FreeToken issue #751, §What we changed: "chunks of up to 16 KiB,
@@ -79,6 +79,15 @@ typedef enum kvx_variant {
     KVX_VARIANT_LDG = 1,  /* 16-byte loads/stores by every lane, several in flight */
     KVX_VARIANT_BULK = 2  /* cp.async.bulk through a shared::cta ring, one issuing lane */
 } kvx_variant;
+
+/* How the LDG kernel hands work units (one warp pass over a chunk) to warps. */
+typedef enum kvx_assign {
+    KVX_ASSIGN_AUTO = 0,    /* the table's choice: DYNAMIC for H2D and D2H, STATIC for D2D */
+    KVX_ASSIGN_STATIC = 1,  /* unit u to warp u mod (warps in the grid) */
+    KVX_ASSIGN_DYNAMIC = 2  /* each warp takes its next unit from a counter kept in the chunk
+                               table's device allocation, so warps the link serves faster take
+                               more units; two copies over the same table must not overlap */
+} kvx_assign;
 
 typedef enum kvx_status {
     KVX_OK = 0,
@@ -113,6 +122,7 @@ typedef struct kvx_launch {
     int stages;          /* BULK: shared-memory ring of stages x KVX_CHUNK_BYTES, 2..12; it is cut
                             into stages of the batch's longest chunk (at most 32 stages) */
     int store_policy;    /* LDG: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
+    int assign;          /* LDG: kvx_assign */
 } kvx_launch;
 
 /* Opaque, library-owned reusable descriptor buffer (device chunk table plus
@@ -160,7 +170,11 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
 
 /* Launch the copy kernel over the uploaded table. No host work besides the
  * launch: fixed shape, allowed inside CUDA graph capture. `cta_budget` as in
- * kvx_copy_batch. */
+ * kvx_copy_batch. Two copies of one buffer must not run at the same time (a
+ * dynamic-assignment copy keeps its work counter in the buffer): outside
+ * capture, a copy on another stream than the buffer's previous copy first
+ * makes `stream` wait for that copy; graph replays are the caller's to
+ * order. */
 kvx_status kvx_copy_uploaded(kvx_desc_buf *buf, int cta_budget, void *stream);
 
 /* kvx_copy_uploaded with an explicit launch configuration (NULL = table). */

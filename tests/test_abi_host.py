@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version_and_status_strings():
-    assert kvx.kvx_version() == 1
+    assert kvx.kvx_version() == kvx.KVX_VERSION == 2
     names = [kvx.status_string(s) for s in range(10)]
     assert names[0] == "KVX_OK" and names[7] == "KVX_ERR_TIMEOUT" and names[9] == "KVX_ERR_CAPTURE"
     assert kvx.status_string(99) == "KVX_ERR_UNKNOWN"
@@ -216,7 +216,7 @@ def test_copy_batch_rejects_before_any_cuda_call():
 
 @pytest.mark.parametrize("launch", [
     {"variant": 3}, {"threads": 1024}, {"threads": 96}, {"unroll": 3}, {"stages": 13},
-    {"store_policy": 3}, {"cta_budget": -2},
+    {"store_policy": 3}, {"cta_budget": -2}, {"assign": 3}, {"assign": -1},
 ])
 def test_copy_batch_ex_rejects_bad_launch(launch):
     s, d, z = _ok_batch()
@@ -232,6 +232,9 @@ def test_default_launch_table():
             assert l["variant"] in (kvx.KVX_VARIANT_LDG, kvx.KVX_VARIANT_BULK)
             assert l["cta_budget"] > 0 and l["threads"] in (128, 256, 512)
             assert l["unroll"] in (2, 4, 8) and 2 <= l["stages"] <= 12
+            # units from a counter over the host link, by position for D2D
+            want = kvx.KVX_ASSIGN_STATIC if dname == "d2d" else kvx.KVX_ASSIGN_DYNAMIC
+            assert l["assign"] == want
     with pytest.raises(kvx.KvxError):
         kvx.kvx_default_launch(5, 4096)
 
@@ -323,22 +326,27 @@ def _run_with_env(code, **env_vars):
 
 def test_kvx_table_file_overrides_rows(tmp_path):
     table = tmp_path / "gb300.table"
-    table.write_text("# dir max_mean variant budget threads unroll stages policy\n"
+    table.write_text("# dir max_mean variant budget threads unroll stages policy [assign]\n"
                      "h2d 8192 bulk 7 256 8 5 0\n"
-                     "h2d inf ldg 33 512 4 3 1\n")
+                     "h2d inf ldg 33 512 4 3 1 static\n"
+                     "d2d inf ldg 99 512 8 3 0 dynamic\n")
     code = ("from expert_host_block_gb300 import kvx\n"
             "print(kvx.kvx_default_launch('h2d', 4096))\n"
             "print(kvx.kvx_default_launch('h2d', 16384))\n"
-            "print(kvx.kvx_default_launch('d2h', 4096))\n")
+            "print(kvx.kvx_default_launch('d2h', 4096))\n"
+            "print(kvx.kvx_default_launch('d2d', 4096))\n")
     out = _run_with_env(code, KVX_TABLE=str(table))
     lines = out.stdout.strip().splitlines()
     assert "'variant': 2, 'cta_budget': 7" in lines[0] and "'stages': 5" in lines[0], out.stderr
-    assert "'cta_budget': 33, 'threads': 512, 'unroll': 4" in lines[1]
+    assert "'assign': 2" in lines[0]  # no assign column: the built-in choice for h2d
+    assert "'cta_budget': 33, 'threads': 512, 'unroll': 4" in lines[1] and "'assign': 1" in lines[1]
     assert "'variant': 1, 'cta_budget': 64" in lines[2]  # no d2h row in the file: built-in row
+    assert "'cta_budget': 99" in lines[3] and "'assign': 2" in lines[3]
 
 
 @pytest.mark.parametrize("text", ["h2d 4096 tma 8 256 8 3 0\n", "h2d 4096 ldg 8 300 8 3 0\n",
-                                  "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n"])
+                                  "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n",
+                                  "h2d inf ldg 8 256 8 3 0 greedy\n"])
 def test_kvx_table_malformed_is_an_error(tmp_path, text):
     table = tmp_path / "bad.table"
     table.write_text(text)

@@ -3,7 +3,8 @@
 Each case draws (from its seed) a descriptor count, sizes that are multiples
 of 8 from 8 bytes to 100 KiB (a quarter of them one-chunk 4 KiB pages, some
 zero), independent 0/8 start phases, disjoint destinations, possibly
-overlapping sources, and a launch configuration; the whole destination pool
+overlapping sources, and a launch configuration (variant, grid, threads,
+loads in flight, store policy, work assignment); the whole destination pool
 must equal the oracle's.
 """
 
@@ -42,7 +43,7 @@ def _random_case(seed):
     launch = {"variant": str(g.choice(["ldg", "bulk"])), "cta_budget": int(g.choice([1, 3, 16, 64, 300]))}
     if launch["variant"] == "ldg":
         launch.update(threads=int(g.choice([128, 256, 512])), unroll=int(g.choice([2, 4, 8])),
-                      store_policy=int(g.integers(0, 3)))
+                      store_policy=int(g.integers(0, 3)), assign=int(g.integers(0, 3)))
     else:
         launch["stages"] = int(g.integers(2, 13))
     ws = "host" if direction == "h2d" else "device"
