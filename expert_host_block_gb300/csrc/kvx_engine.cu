@@ -1212,9 +1212,14 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     return KVX_OK;
 }
 
-kvx_status kvx_status_enqueue(void *stream_, kvx_status_token *tok)
+namespace {
+
+// Queue a read of the status word behind the work on `stream`. With `side`
+// (and outside a capture) the read runs on the status side stream, so later
+// work on `stream` does not wait for it; otherwise it is a launch on `stream`,
+// which reaches the host sooner when the caller waits for it at once.
+kvx_status status_enqueue(cudaStream_t stream, kvx_status_token *tok, bool side)
 {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!tok)
         return fail(KVX_ERR_INVALID_ARG, "null token");
     int dev = 0;
@@ -1236,24 +1241,31 @@ kvx_status kvx_status_enqueue(void *stream_, kvx_status_token *tok)
     if (!w.marks[slot])
         KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.marks[slot], cudaEventDisableTiming));
     w.words[slot] = 0;
-    if (cap) {
+    if (cap || !side) {
         // inside a capture the read becomes a node of the graph
         KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, stream));
         KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
     } else {
         // the read waits for the work already on `stream`, on a side stream,
         // so that the next copy on `stream` does not wait for the read
-        cudaStream_t side = nullptr;
-        KVX_CUDA_TRY(aux_stream(dev, kAuxStatus, &side));
+        cudaStream_t aux = nullptr;
+        KVX_CUDA_TRY(aux_stream(dev, kAuxStatus, &aux));
         KVX_CUDA_TRY(cudaEventRecord(w.marks[slot], stream));
-        KVX_CUDA_TRY(cudaStreamWaitEvent(side, w.marks[slot], 0));
-        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, side));
-        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], side));
+        KVX_CUDA_TRY(cudaStreamWaitEvent(aux, w.marks[slot], 0));
+        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, aux));
+        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], aux));
     }
     tok->slot = slot;
     tok->gen = ++w.gen[slot];
     tok->device = dev;
     return KVX_OK;
+}
+
+}  // namespace
+
+kvx_status kvx_status_enqueue(void *stream, kvx_status_token *tok)
+{
+    return status_enqueue(static_cast<cudaStream_t>(stream), tok, true);
 }
 
 namespace {
@@ -1305,7 +1317,7 @@ kvx_status kvx_status_wait(const kvx_status_token *tok)
 kvx_status kvx_stream_check(void *stream)
 {
     kvx_status_token tok;
-    kvx_status st = kvx_status_enqueue(stream, &tok);
+    kvx_status st = status_enqueue(static_cast<cudaStream_t>(stream), &tok, false);
     if (st != KVX_OK)
         return st;
     return kvx_status_wait(&tok);

@@ -46,6 +46,10 @@ struct Launch {
 // keeps it zero) and after every copy (the last warp zeroes it).
 constexpr size_t kTableHeader = 1;
 
+// KVX_ASSIGN_DYNAMIC applies to launches with at least this many work units
+// per warp; smaller ones are assigned by position.
+constexpr uint64_t kDynamicMinUnitsPerWarp = 8;
+
 // Grid needed to give every CTA some work, for a chunk count, the longest
 // chunk and the variant.
 int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);

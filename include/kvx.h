@@ -86,7 +86,9 @@ typedef enum kvx_assign {
     KVX_ASSIGN_STATIC = 1,  /* unit u to warp u mod (warps in the grid) */
     KVX_ASSIGN_DYNAMIC = 2  /* each warp takes its next unit from a counter kept in the chunk
                                table's device allocation, so warps the link serves faster take
-                               more units; two copies over the same table must not overlap */
+                               more units; two copies over the same table must not overlap.
+                               Applies when there are at least 8 units per warp (fewer go by
+                               position) */
 } kvx_assign;
 
 typedef enum kvx_status {

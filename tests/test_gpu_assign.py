@@ -53,7 +53,7 @@ def _recanary(p):
 @pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
 @pytest.mark.parametrize("n,budget", [(3, 64), (500, 16), (4000, 64), (4000, 300)])
 def test_table_reused_with_dynamic_assignment(direction, n, budget):
-    # (3, 64): far more warps than units; most warps take nothing
+    # (3, 64): under 8 units a warp, so assigned by position even when dynamic is asked
     specs, b = _case(direction, n, n + budget)
     p = Pools(specs)
     buf = kvx.DescBuf(max(1, int(sum(-(-int(x) // 16384) for x in b.sizes))))
