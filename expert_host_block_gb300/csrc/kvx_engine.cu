@@ -273,16 +273,18 @@ kvx_status check_kinds(const uint64_t *src, const uint64_t *dst, const uint64_t 
     return KVX_OK;
 }
 
-// Validate; count chunks and payload bytes, and find the longest chunk.
+// Validate; count chunks and payload bytes, find the longest chunk, and count
+// the bytes of descriptors whose source, destination and size are all
+// multiples of 16 (the bulk copy's condition).
 kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
                     int dir, int level, uint64_t *n_chunks, uint64_t *payload,
-                    uint32_t *max_chunk = nullptr)
+                    uint32_t *max_chunk = nullptr, uint64_t *aligned16 = nullptr)
 {
     if (dir < KVX_H2D || dir > KVX_D2D)
         return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
     if (level < 0 || level > 2)
         return fail(KVX_ERR_INVALID_ARG, "validation level %d is not 0, 1 or 2", level);
-    uint64_t chunks = 0, bytes = 0, longest = 0;
+    uint64_t chunks = 0, bytes = 0, longest = 0, aligned = 0;
     if (n) {
         if (!src || !dst || !sizes)
             return fail(KVX_ERR_INVALID_ARG, "null descriptor array with n = %zu", n);
@@ -298,6 +300,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
                            ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d) | (z > kHuge)) << 3));
             chunks += (z >> 14) + ((z & (KVX_CHUNK_BYTES - 1)) != 0);
             bytes += z;
+            aligned += ((s | d | z) & 15u) ? 0 : z;
             longest = z > longest ? z : longest;
         }
         if (!bad) {
@@ -305,7 +308,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
                 return fail(KVX_ERR_CAPACITY, "batch needs more than KVX_MAX_CHUNKS (%u) chunks",
                             KVX_MAX_CHUNKS);
         } else {
-            chunks = bytes = longest = 0;
+            chunks = bytes = longest = aligned = 0;
         }
         for (size_t i = 0; bad && i < n; ++i) {
             const uint64_t z = sizes[i];
@@ -325,6 +328,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
                             (unsigned long long)z);
             chunks += chunks_of(z);
             bytes += z;
+            aligned += ((s | d | z) & 15u) ? 0 : z;
             if (z > longest)
                 longest = z;
             if (chunks > KVX_MAX_CHUNKS)
@@ -348,6 +352,8 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
         *payload = bytes;
     if (max_chunk)
         *max_chunk = (uint32_t)std::min<uint64_t>(longest, KVX_CHUNK_BYTES);
+    if (aligned16)
+        *aligned16 = aligned;
     return KVX_OK;
 }
 
@@ -377,29 +383,31 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
 // check or is longer than one chunk; the caller then takes the exact two-pass
 // path, which also reports the first failing descriptor.
 struct PackAcc {
-    uint64_t bad = 0, bytes = 0, longest = 0;
+    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0;
 };
 
 void pack_fast_range(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t a, size_t b,
                      kvx_chunk *out, PackAcc &acc)
 {
-    uint64_t bad = 0, bytes = 0, longest = 0;
+    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0;
     for (size_t i = a; i < b; ++i) {
         const uint64_t z = sizes[i], s = src[i], d = dst[i];
         const uint64_t live = z ? ~0ull : 0ull;
         bad |= live & (((s | d | z) & 7u) | ((uint64_t)((s == 0) | (d == 0) | (s + z < s) | (d + z < d)) << 3));
         bad |= (uint64_t)(z > KVX_CHUNK_BYTES) << 4;
         bytes += z;
+        aligned += ((s | d | z) & 15u) ? 0 : z;
         longest = z > longest ? z : longest;
         out[i] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
     }
     acc.bad = bad;
     acc.bytes = bytes;
     acc.longest = longest;
+    acc.aligned = aligned;
 }
 
 bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
-               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk)
+               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk, uint64_t *aligned16)
 {
     // Large batches are split over the calling thread and the worker pool.
     constexpr size_t kParallelMin = 8192, kMinPart = 4096;
@@ -421,12 +429,14 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
         t.bad |= acc[p].bad;
         t.bytes += acc[p].bytes;
         t.longest = std::max(t.longest, acc[p].longest);
+        t.aligned += acc[p].aligned;
     }
     if (t.bad || n > KVX_MAX_CHUNKS)
         return false;
     *n_chunks = n;
     *payload = t.bytes;
     *max_chunk = (uint32_t)t.longest;
+    *aligned16 = t.aligned;
     return true;
 }
 
@@ -452,19 +462,27 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // unchanged or up to 1.5 % faster). D2D keeps the assignment by position: its
 // units take ~1 us, so one counter shared by 2,432 warps contends (4 KiB x
 // 65,536 chunks: 2.1 against 3.2 TB/s).
+//
+// A BULK row applies only to a batch whose bytes are at least 90 % in
+// descriptors with 16-byte aligned source, destination and size: the bulk
+// kernel moves every other chunk with its single warp, which for D2D chunks of
+// 16-28 KiB with 8-byte tails ran at 0.75 TB/s where LDG reaches 3.
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2D, 12287, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 608, 256, 8, 6, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 
 int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
 
-kvx_launch table_launch(int dir, uint64_t mean_chunk)
+// The row for a batch of this direction and mean chunk size; `aligned` says
+// whether the batch may take a BULK row.
+kvx_launch table_launch(int dir, uint64_t mean_chunk, bool aligned = true)
 {
     for (const TableRow &r : env().table) {  // KVX_TABLE rows first
-        if (r.dir == dir && mean_chunk <= r.max_mean_chunk) {
+        if (r.dir == dir && mean_chunk <= r.max_mean_chunk && (aligned || r.cfg.variant != KVX_VARIANT_BULK)) {
             kvx_launch c = r.cfg;
             if (c.assign == KVX_ASSIGN_AUTO)
                 c.assign = default_assign(dir);
@@ -472,15 +490,18 @@ kvx_launch table_launch(int dir, uint64_t mean_chunk)
         }
     }
     for (const TableRow &r : kTable)
-        if (r.dir == dir && mean_chunk <= r.max_mean_chunk)
+        if (r.dir == dir && mean_chunk <= r.max_mean_chunk && (aligned || r.cfg.variant != KVX_VARIANT_BULK))
             return r.cfg;
     return kTable[0].cfg;
 }
 
+// Whether a batch is aligned enough for a BULK row (see the table).
+bool mostly_aligned(uint64_t aligned16, uint64_t payload) { return aligned16 * 10 >= payload * 9; }
+
 // Merge explicit settings over env over table and check them.
-kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch *out)
+kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch *out, bool aligned = true)
 {
-    kvx_launch t = table_launch(dir, mean_chunk);
+    kvx_launch t = table_launch(dir, mean_chunk, aligned);
     const EnvSettings &e = env();
     int variant = (want && want->variant) ? want->variant : (e.variant ? e.variant : t.variant);
     int budget = (want && want->cta_budget) ? want->cta_budget : (e.cta_budget ? e.cta_budget : t.cta_budget);
@@ -754,12 +775,12 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     Slot *s = nullptr;
     if (ring_acquire(dev, n, &s) != KVX_OK)
         return KVX_OK;
-    uint64_t chunks = 0, payload = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0;
     uint32_t max_chunk = 0;
     Launch l;
-    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk) ||
+    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk, &aligned16) ||
         payload == 0 ||
-        resolve(dir, payload / chunks, want, &l) != KVX_OK) {
+        resolve(dir, payload / chunks, want, &l, mostly_aligned(aligned16, payload)) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;
     }
@@ -897,13 +918,13 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
         if (done)
             return st;
     }
-    uint64_t chunks = 0, payload = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
     if (st != KVX_OK)
         return st;
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, want, &l);
+    st = resolve(dir, chunks ? payload / chunks : 0, want, &l, mostly_aligned(aligned16, payload));
     if (st != KVX_OK)
         return st;
     if (chunks == 0)
@@ -991,16 +1012,16 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
-    uint64_t chunks = 0, payload = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
     if (st != KVX_OK)
         return st;
     if (chunks > b->cap)
         return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, buffer holds %zu",
                     (unsigned long long)chunks, b->cap);
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, nullptr, &l);
+    st = resolve(dir, chunks ? payload / chunks : 0, nullptr, &l, mostly_aligned(aligned16, payload));
     if (st != KVX_OK)
         return st;
     bool cap = false;
@@ -1469,9 +1490,9 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
-    uint64_t chunks = 0, payload = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
     if (st != KVX_OK)
         return st;
     if (chunks > KVX_NOALLOC_MAX_CHUNKS)
@@ -1481,7 +1502,7 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_launch want{};
     want.cta_budget = cta_budget;
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, &want, &l);
+    st = resolve(dir, chunks ? payload / chunks : 0, &want, &l, mostly_aligned(aligned16, payload));
     if (st != KVX_OK)
         return st;
     if (chunks == 0)

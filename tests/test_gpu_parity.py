@@ -550,3 +550,23 @@ def test_status_token_pending_then_timeout_then_expiry():
     with pytest.raises(kvx.KvxError) as e:
         kvx.kvx_status_wait(old)
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("odd", [False, True])
+def test_d2d_table_row_follows_alignment(odd):
+    # 16 KiB D2D chunks take the bulk row only when the batch is 16-byte
+    # aligned; with 8-byte tails and phases they take LDG. Both bit-exact.
+    w = W.sweep_cell(16, 4096, "d2d", odd_tails=odd)
+    (b,) = w.batches
+    p = Pools(w.pools)
+    buf = kvx.DescBuf(int(sum(-(-int(x) // 16384) for x in b.sizes)))
+    try:
+        buf.upload(*p.addrs(b), "d2d")
+        assert buf.info()[2]["variant"] == (kvx.KVX_VARIANT_LDG if odd else kvx.KVX_VARIANT_BULK)
+        want = p.expected([b])
+        buf.copy(stream=None)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        buf.close()
+        p.close()
