@@ -23,6 +23,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cctype>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -77,6 +78,7 @@ struct TableRow {
     int dir;
     uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
     kvx_launch cfg;
+    uint64_t min_payload = 0;  // ... and the batch carries at least this many bytes
 };
 
 struct EnvSettings {
@@ -89,10 +91,11 @@ struct EnvSettings {
 };
 
 // A launch table in a text file: one row per line, `#` starts a comment:
-//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy [assign]
+//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy [assign [min_payload_bytes]]
 // with dir h2d|d2h|d2d, max_mean_chunk_bytes an integer or "inf", variant
-// ldg|bulk, assign static|dynamic (absent: the built-in choice for dir).
-// Rows are tried in file order, before the built-in rows.
+// ldg|bulk, assign static|dynamic|auto (absent or auto: the built-in choice
+// for dir), min_payload_bytes an integer (absent: 0). Rows are tried in file
+// order, before the built-in rows.
 std::string parse_table(const char *path, std::vector<TableRow> *rows)
 {
     FILE *f = fopen(path, "r");
@@ -105,10 +108,10 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         ++lineno;
         if (char *h = strchr(line, '#'))
             *h = 0;
-        char dir[16], maxs[32], var[16], asg[16] = "";
+        char dir[16], maxs[32], var[16], asg[16] = "", minp[32] = "";
         int budget, threads, unroll, stages, policy;
-        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s", dir, maxs, var, &budget, &threads,
-                               &unroll, &stages, &policy, asg);
+        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s %31s", dir, maxs, var, &budget, &threads,
+                               &unroll, &stages, &policy, asg, minp);
         if (got <= 0)
             continue;  // blank or comment
         TableRow r{};
@@ -119,14 +122,19 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         else
             r.max_mean_chunk = strtoull(maxs, &end, 10);
         const int variant = !strcmp(var, "ldg") ? KVX_VARIANT_LDG : !strcmp(var, "bulk") ? KVX_VARIANT_BULK : -1;
-        const int assign = got < 9 ? KVX_ASSIGN_AUTO
+        const int assign = (got < 9 || !strcmp(asg, "auto")) ? KVX_ASSIGN_AUTO
                            : !strcmp(asg, "static") ? KVX_ASSIGN_STATIC
                            : !strcmp(asg, "dynamic") ? KVX_ASSIGN_DYNAMIC : -1;
+        char *pend = nullptr;
+        if (got >= 10)
+            r.min_payload = strtoull(minp, &pend, 10);
         if (got < 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
             (threads != 128 && threads != 256 && threads != 512) || (unroll != 2 && unroll != 4 && unroll != 8) ||
-            stages < 2 || stages > 12 || policy < 0 || policy > 2 || assign < 0) {
+            stages < 2 || stages > 12 || policy < 0 || policy > 2 || assign < 0 || (pend && *pend) ||
+            (got >= 10 && !isdigit((unsigned char)minp[0]))) {
             err = std::string("KVX_TABLE=") + path + ": line " + std::to_string(lineno) +
-                  " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy [assign]'";
+                  " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy "
+                  "[assign [min_payload]]'";
             break;
         }
         r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy, assign};
@@ -467,22 +475,42 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // descriptors with 16-byte aligned source, destination and size: the bulk
 // kernel moves every other chunk with its single warp, which for D2D chunks of
 // 16-28 KiB with 8-byte tails ran at 0.75 TB/s where LDG reaches 3.
+//
+// D2D, from the mean of 30 L2-flushed launches per shape (the event timer
+// ticks in ~1 us, so medians of short launches are coarse): the bulk ring is
+// fastest for batches of 256 MiB and more in chunks of 12 KiB and more (16 KiB
+// x 32,768: 0.990 of HBM with 456 CTAs and 96 KiB rings, against 0.963 for
+// LDG), and LDG with 256-thread CTAs for everything else (16 KiB x 4,096:
+// 0.970 against 0.894 for the ring, whose fill and drain do not amortise over
+// 64 MiB; 4 KiB x 65,536: 0.958 against 0.935 for 512-thread CTAs).
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
-    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 608, 256, 8, 6, 0, KVX_ASSIGN_STATIC}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 608, 256, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 608, 256, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 
 int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
 
-// The row for a batch of this direction and mean chunk size; `aligned` says
-// whether the batch may take a BULK row.
-kvx_launch table_launch(int dir, uint64_t mean_chunk, bool aligned = true)
+// The shape of a batch that the table rows look at.
+struct BatchShape {
+    uint64_t mean_chunk = 0;        // payload / chunks
+    uint64_t payload = ~0ull;       // bytes (unknown: as large as can be)
+    bool aligned = true;            // may take a BULK row
+};
+
+bool row_matches(const TableRow &r, int dir, const BatchShape &b)
+{
+    return r.dir == dir && b.mean_chunk <= r.max_mean_chunk && b.payload >= r.min_payload &&
+           (b.aligned || r.cfg.variant != KVX_VARIANT_BULK);
+}
+
+// The row for a batch of this direction and shape.
+kvx_launch table_launch(int dir, const BatchShape &b)
 {
     for (const TableRow &r : env().table) {  // KVX_TABLE rows first
-        if (r.dir == dir && mean_chunk <= r.max_mean_chunk && (aligned || r.cfg.variant != KVX_VARIANT_BULK)) {
+        if (row_matches(r, dir, b)) {
             kvx_launch c = r.cfg;
             if (c.assign == KVX_ASSIGN_AUTO)
                 c.assign = default_assign(dir);
@@ -490,18 +518,26 @@ kvx_launch table_launch(int dir, uint64_t mean_chunk, bool aligned = true)
         }
     }
     for (const TableRow &r : kTable)
-        if (r.dir == dir && mean_chunk <= r.max_mean_chunk && (aligned || r.cfg.variant != KVX_VARIANT_BULK))
+        if (row_matches(r, dir, b))
             return r.cfg;
     return kTable[0].cfg;
 }
 
-// Whether a batch is aligned enough for a BULK row (see the table).
-bool mostly_aligned(uint64_t aligned16, uint64_t payload) { return aligned16 * 10 >= payload * 9; }
+// The shape of a validated batch: whether it is aligned enough for a BULK row
+// (see the table), its mean chunk and its payload.
+BatchShape batch_shape(uint64_t chunks, uint64_t payload, uint64_t aligned16)
+{
+    BatchShape b;
+    b.mean_chunk = chunks ? payload / chunks : 0;
+    b.payload = payload;
+    b.aligned = aligned16 / 9 >= payload / 10;  // at least ~90 % (no overflow near 2^64)
+    return b;
+}
 
 // Merge explicit settings over env over table and check them.
-kvx_status resolve(int dir, uint64_t mean_chunk, const kvx_launch *want, Launch *out, bool aligned = true)
+kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Launch *out)
 {
-    kvx_launch t = table_launch(dir, mean_chunk, aligned);
+    kvx_launch t = table_launch(dir, shape);
     const EnvSettings &e = env();
     int variant = (want && want->variant) ? want->variant : (e.variant ? e.variant : t.variant);
     int budget = (want && want->cta_budget) ? want->cta_budget : (e.cta_budget ? e.cta_budget : t.cta_budget);
@@ -780,7 +816,7 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     Launch l;
     if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk, &aligned16) ||
         payload == 0 ||
-        resolve(dir, payload / chunks, want, &l, mostly_aligned(aligned16, payload)) != KVX_OK) {
+        resolve(dir, batch_shape(chunks, payload, aligned16), want, &l) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;
     }
@@ -901,7 +937,9 @@ kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *ou
         return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
     if (!out)
         return fail(KVX_ERR_INVALID_ARG, "null output");
-    *out = table_launch(dir, mean_chunk_bytes);
+    BatchShape b;
+    b.mean_chunk = mean_chunk_bytes;
+    *out = table_launch(dir, b);
     return KVX_OK;
 }
 
@@ -924,7 +962,7 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     if (st != KVX_OK)
         return st;
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, want, &l, mostly_aligned(aligned16, payload));
+    st = resolve(dir, batch_shape(chunks, payload, aligned16), want, &l);
     if (st != KVX_OK)
         return st;
     if (chunks == 0)
@@ -1021,7 +1059,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
         return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, buffer holds %zu",
                     (unsigned long long)chunks, b->cap);
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, nullptr, &l, mostly_aligned(aligned16, payload));
+    st = resolve(dir, batch_shape(chunks, payload, aligned16), nullptr, &l);
     if (st != KVX_OK)
         return st;
     bool cap = false;
@@ -1078,7 +1116,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
             merged.assign = want->assign;
     }
     Launch l;
-    st = resolve(b->dir, 0, &merged, &l);
+    st = resolve(b->dir, BatchShape{}, &merged, &l);
     if (st != KVX_OK)
         return st;
     if (b->n_chunks == 0)
@@ -1201,7 +1239,7 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     // row for the direction (its small-chunk row) and apply the caller's fields.
     if (want && want->variant && want->variant != KVX_VARIANT_LDG)
         return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
-    kvx_launch merged = table_launch(dir, 0);
+    kvx_launch merged = table_launch(dir, BatchShape{});
     if (want) {
         if (want->cta_budget < 0)
             return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", want->cta_budget);
@@ -1216,7 +1254,7 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     }
     merged.variant = KVX_VARIANT_LDG;
     Launch lc;
-    st = resolve(dir, 0, &merged, &lc);
+    st = resolve(dir, BatchShape{}, &merged, &lc);
     if (st != KVX_OK)
         return st;
     bool cap = false;
@@ -1502,7 +1540,7 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_launch want{};
     want.cta_budget = cta_budget;
     Launch l;
-    st = resolve(dir, chunks ? payload / chunks : 0, &want, &l, mostly_aligned(aligned16, payload));
+    st = resolve(dir, batch_shape(chunks, payload, aligned16), &want, &l);
     if (st != KVX_OK)
         return st;
     if (chunks == 0)

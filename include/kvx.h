@@ -300,10 +300,12 @@ kvx_status kvx_plan_chunks(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                            size_t max_out, size_t *n_chunks);
 
 /* The calibrated launch configuration for a direction and mean chunk size,
- * for a batch of 16-byte aligned descriptors. A row that selects
- * KVX_VARIANT_BULK applies only to batches with at least 90 % of their bytes
- * in descriptors whose source, destination and size are multiples of 16; other
- * batches take the next matching row. */
+ * for a large batch of 16-byte aligned descriptors. Rows are chosen by
+ * direction, mean chunk size and, for some rows, the batch's payload (the D2D
+ * bulk row needs 256 MiB or more). A row that selects KVX_VARIANT_BULK applies
+ * only to batches with at least 90 % of their bytes in descriptors whose
+ * source, destination and size are multiples of 16; other batches take the
+ * next matching row. */
 kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *out);
 
 /* Process-wide validation level for kvx_copy_batch / kvx_upload_descriptors

@@ -329,6 +329,7 @@ def test_kvx_table_file_overrides_rows(tmp_path):
     table.write_text("# dir max_mean variant budget threads unroll stages policy [assign]\n"
                      "h2d 8192 bulk 7 256 8 5 0\n"
                      "h2d inf ldg 33 512 4 3 1 static\n"
+                     "d2d inf bulk 11 256 8 4 0 auto 1099511627776\n"  # batches of 1 TiB and more
                      "d2d inf ldg 99 512 8 3 0 dynamic\n")
     code = ("from expert_host_block_gb300 import kvx\n"
             "print(kvx.kvx_default_launch('h2d', 4096))\n"
@@ -341,12 +342,13 @@ def test_kvx_table_file_overrides_rows(tmp_path):
     assert "'assign': 2" in lines[0]  # no assign column: the built-in choice for h2d
     assert "'cta_budget': 33, 'threads': 512, 'unroll': 4" in lines[1] and "'assign': 1" in lines[1]
     assert "'variant': 1, 'cta_budget': 64" in lines[2]  # no d2h row in the file: built-in row
-    assert "'cta_budget': 99" in lines[3] and "'assign': 2" in lines[3]
+    # kvx_default_launch describes a large batch: the 1 TiB row applies (assign auto: static for d2d)
+    assert "'variant': 2, 'cta_budget': 11" in lines[3] and "'assign': 1" in lines[3]
 
 
 @pytest.mark.parametrize("text", ["h2d 4096 tma 8 256 8 3 0\n", "h2d 4096 ldg 8 300 8 3 0\n",
                                   "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n",
-                                  "h2d inf ldg 8 256 8 3 0 greedy\n"])
+                                  "h2d inf ldg 8 256 8 3 0 greedy\n", "h2d inf ldg 8 256 8 3 0 auto 12x\n"])
 def test_kvx_table_malformed_is_an_error(tmp_path, text):
     table = tmp_path / "bad.table"
     table.write_text(text)

@@ -552,17 +552,17 @@ def test_status_token_pending_then_timeout_then_expiry():
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("odd", [False, True])
-def test_d2d_table_row_follows_alignment(odd):
-    # 16 KiB D2D chunks take the bulk row only when the batch is 16-byte
-    # aligned; with 8-byte tails and phases they take LDG. Both bit-exact.
-    w = W.sweep_cell(16, 4096, "d2d", odd_tails=odd)
+@pytest.mark.parametrize("n,odd,variant", [(4096, False, "ldg"), (32768, False, "bulk"), (32768, True, "ldg")])
+def test_d2d_table_row_follows_shape(n, odd, variant):
+    # 16 KiB D2D chunks take the bulk row only for a batch of 256 MiB or more
+    # that is 16-byte aligned; 64 MiB, or 8-byte tails and phases, take LDG.
+    w = W.sweep_cell(16, n, "d2d", odd_tails=odd)
     (b,) = w.batches
     p = Pools(w.pools)
     buf = kvx.DescBuf(int(sum(-(-int(x) // 16384) for x in b.sizes)))
     try:
         buf.upload(*p.addrs(b), "d2d")
-        assert buf.info()[2]["variant"] == (kvx.KVX_VARIANT_LDG if odd else kvx.KVX_VARIANT_BULK)
+        assert buf.info()[2]["variant"] == kvx.VARIANTS[variant]
         want = p.expected([b])
         buf.copy(stream=None)
         kvx.kvx_stream_check(None)
