@@ -852,7 +852,6 @@ struct kvx_desc_buf {
     kvx_chunk *host = nullptr;  // pinned staging, same layout (header kept zero)
     cudaEvent_t upload_done = nullptr;
     cudaEvent_t last_use = nullptr;
-    cudaStream_t last_stream = nullptr;  // stream of the last copy
     bool upload_recorded = false;
     bool use_recorded = false;
     uint32_t n_chunks = 0;
@@ -1126,8 +1125,10 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     if (st != KVX_OK)
         return st;
     // two copies over one table must not overlap: order this one after the
-    // buffer's previous copy when that ran on another stream
-    if (!cap && b->use_recorded && b->last_stream != stream)
+    // buffer's previous copy (a no-op when that ran earlier on this stream;
+    // stream handles are not compared, since a destroyed stream's handle can
+    // come back for a new one)
+    if (!cap && b->use_recorded)
         KVX_CUDA_TRY(cudaStreamWaitEvent(stream, b->last_use, 0));
     cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, stream);
     if (e != cudaSuccess)
@@ -1135,7 +1136,6 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     if (!cap) {
         KVX_CUDA_TRY(cudaEventRecord(b->last_use, stream));
         b->use_recorded = true;
-        b->last_stream = stream;
     }
     return KVX_OK;
 }

@@ -174,8 +174,8 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
  * launch: fixed shape, allowed inside CUDA graph capture. `cta_budget` as in
  * kvx_copy_batch. Two copies of one buffer must not run at the same time (a
  * dynamic-assignment copy keeps its work counter in the buffer): outside
- * capture, a copy on another stream than the buffer's previous copy first
- * makes `stream` wait for that copy; graph replays are the caller's to
+ * capture, each copy first makes `stream` wait for the buffer's previous copy
+ * (free when that was on the same stream); graph replays are the caller's to
  * order. */
 kvx_status kvx_copy_uploaded(kvx_desc_buf *buf, int cta_budget, void *stream);
 
