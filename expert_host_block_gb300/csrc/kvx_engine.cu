@@ -942,6 +942,36 @@ kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *ou
     return KVX_OK;
 }
 
+kvx_status kvx_select_launch(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
+                             int dir, const kvx_launch *want, kvx_launch *out)
+{
+    if (!out)
+        return fail(KVX_ERR_INVALID_ARG, "null output");
+    kvx_status st = check_env();
+    if (st != KVX_OK)
+        return st;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint32_t max_chunk = 0;
+    st = validate(src, dst, sizes, n, dir, 0, &chunks, &payload, &max_chunk, &aligned16);
+    if (st != KVX_OK)
+        return st;
+    Launch l;
+    st = resolve(dir, batch_shape(chunks, payload, aligned16), want, &l);
+    if (st != KVX_OK)
+        return st;
+    const bool ldg = l.variant == KVX_VARIANT_LDG;
+    *out = kvx_launch{l.variant,
+                      chunks ? kvx::work_ctas(l, (uint32_t)chunks, max_chunk) : 0,
+                      ldg ? l.threads : 0,
+                      ldg ? l.unroll : 0,
+                      ldg ? 0 : l.stages,
+                      ldg ? l.store_policy : 0,
+                      ldg ? (kvx::ldg_dynamic(l, (uint32_t)chunks, max_chunk) ? KVX_ASSIGN_DYNAMIC
+                                                                             : KVX_ASSIGN_STATIC)
+                          : 0};
+    return KVX_OK;
+}
+
 kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
                              int dir, const kvx_launch *want, void *stream_)
 {

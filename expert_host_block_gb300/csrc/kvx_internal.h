@@ -54,6 +54,10 @@ constexpr uint64_t kDynamicMinUnitsPerWarp = 8;
 // chunk and the variant.
 int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
 
+// Whether an LDG launch takes its units from the table's counter: asked for
+// (KVX_ASSIGN_DYNAMIC) and at least kDynamicMinUnitsPerWarp units per warp.
+bool ldg_dynamic(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
+
 // Enqueue the copy kernel over a device-resident chunk table: `table` points at
 // its header record, n_chunks records follow. max_chunk_len is the longest
 // record's len (it sets the LDG kernel's passes per chunk).

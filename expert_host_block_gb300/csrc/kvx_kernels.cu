@@ -826,6 +826,17 @@ uint32_t ldg_passes(const Launch &l, uint32_t max_chunk_len)
     return p ? p : 1u;
 }
 
+// A counter pays off only when every warp has many units to balance; with a
+// few units a warp (1,024 x 4 KiB over 512 warps: 2) the positional split,
+// with its 32-record batches, is faster (146 against 141 GB/s).
+bool ldg_dynamic(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
+{
+    if (l.variant != KVX_VARIANT_LDG || l.assign != KVX_ASSIGN_DYNAMIC)
+        return false;
+    const uint64_t warps = (uint64_t)work_ctas(l, n_chunks, max_chunk_len) * (uint64_t)(l.threads / 32);
+    return (uint64_t)n_chunks * ldg_passes(l, max_chunk_len) >= kDynamicMinUnitsPerWarp * warps;
+}
+
 int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
 {
     uint64_t need;
@@ -851,13 +862,8 @@ cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
         return launch_bulk(ctas, l.stages, recs, n_chunks, max_chunk_len, stream);
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
-    // A counter pays off only when every warp has many units to balance; with
-    // a few units a warp (1,024 x 4 KiB over 512 warps: 2) the positional
-    // split, with its 32-record batches, is faster (146 against 141 GB/s).
-    const uint64_t warps = (uint64_t)ctas * (uint64_t)(l.threads / 32);
-    const bool dynamic = l.assign == KVX_ASSIGN_DYNAMIC &&
-                         (uint64_t)n_chunks * passes >= kDynamicMinUnitsPerWarp * warps;
-    unsigned long long *ctr = dynamic ? reinterpret_cast<unsigned long long *>(table) : nullptr;
+    unsigned long long *ctr =
+        ldg_dynamic(l, n_chunks, max_chunk_len) ? reinterpret_cast<unsigned long long *>(table) : nullptr;
     switch (l.unroll) {
     case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, stream);
     case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, stream);

@@ -42,7 +42,7 @@ KVX_ERR_DEVICE_FAULT = 8
 KVX_ERR_CAPTURE = 9
 
 # the C ABI version this binding's structures follow (KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR)
-KVX_VERSION = 2
+KVX_VERSION = 3
 
 KVX_CHUNK_BYTES = 16384
 KVX_MAX_CHUNKS = 1 << 22
@@ -55,7 +55,7 @@ EXPORTS = (
     "kvx_copy_batch", "kvx_copy_batch_ex", "kvx_desc_buf_create", "kvx_upload_descriptors",
     "kvx_copy_uploaded", "kvx_copy_uploaded_ex", "kvx_desc_buf_info", "kvx_desc_buf_destroy",
     "kvx_validate", "kvx_plan_chunks", "kvx_default_launch", "kvx_set_validate_level",
-    "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version",
+    "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version", "kvx_select_launch",
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
     "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
@@ -114,6 +114,8 @@ def _load():
         "kvx_validate": ([_vp, _vp, _vp, _sz, _int, _int], _int),
         "kvx_plan_chunks": ([_vp, _vp, _vp, _sz, _vp, _sz, ctypes.POINTER(_sz)], _int),
         "kvx_default_launch": ([_int, _u64, ctypes.POINTER(kvx_launch)], _int),
+        "kvx_select_launch": ([_vp, _vp, _vp, _sz, _int, ctypes.POINTER(kvx_launch),
+                               ctypes.POINTER(kvx_launch)], _int),
         "kvx_set_validate_level": ([_int], _int),
         "kvx_get_validate_level": ([], _int),
         "kvx_status_string": ([_int], ctypes.c_char_p),
@@ -476,6 +478,16 @@ def kvx_default_launch(dir, mean_chunk_bytes: int) -> dict:
     l = kvx_launch()
     _check(_load().kvx_default_launch(_dir(dir), int(mean_chunk_bytes), ctypes.byref(l)))
     return l.as_dict()
+
+
+def kvx_select_launch(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, launch=None) -> dict:
+    """The launch kvx_copy_batch_ex would make for this batch (host only, no device needed)."""
+    s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
+    lp = _launch(launch)
+    out = kvx_launch()
+    _check(_load().kvx_select_launch(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
+                                     ctypes.byref(lp) if lp is not None else None, ctypes.byref(out)))
+    return out.as_dict()
 
 
 def kvx_set_validate_level(level: int) -> None:

@@ -59,7 +59,7 @@ extern "C" {
 #endif
 
 #define KVX_VERSION_MAJOR 0
-#define KVX_VERSION_MINOR 2
+#define KVX_VERSION_MINOR 3
 
 /* Largest chunk a descriptor is cut into: 16 KiB, the chunk of the FreeToken
  * gather (FreeToken issue #751, §What we changed: "chunks of up to 16 KiB,
@@ -298,6 +298,18 @@ kvx_status kvx_validate(const uint64_t *src_addrs, const uint64_t *dst_addrs,
 kvx_status kvx_plan_chunks(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                            const uint64_t *sizes, size_t n, kvx_chunk *out,
                            size_t max_out, size_t *n_chunks);
+
+/* The launch kvx_copy_batch_ex(..., want, ...) would make for this batch,
+ * computed on the host without a device: validation level 0, the table row
+ * for the batch's direction, mean chunk, payload and alignment, then the KVX_*
+ * environment and `want` (NULL = none) over it. In *out, cta_budget is the
+ * grid actually launched (at most the budget, at most the work; 0 for an
+ * empty batch); fields the chosen variant does not use are 0; assign is what
+ * the kernel will do (STATIC when DYNAMIC was asked for but the batch has
+ * fewer than 8 units per warp). Same errors as kvx_copy_batch's validation. */
+kvx_status kvx_select_launch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
+                             const uint64_t *sizes, size_t n, int dir, const kvx_launch *want,
+                             kvx_launch *out);
 
 /* The calibrated launch configuration for a direction and mean chunk size,
  * for a large batch of 16-byte aligned descriptors. Rows are chosen by

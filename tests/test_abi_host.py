@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version_and_status_strings():
-    assert kvx.kvx_version() == kvx.KVX_VERSION == 2
+    assert kvx.kvx_version() == kvx.KVX_VERSION == 3
     names = [kvx.status_string(s) for s in range(10)]
     assert names[0] == "KVX_OK" and names[7] == "KVX_ERR_TIMEOUT" and names[9] == "KVX_ERR_CAPTURE"
     assert kvx.status_string(99) == "KVX_ERR_UNKNOWN"
@@ -378,3 +378,74 @@ def test_kvx_log_reports_failures_on_stderr():
            "    print(e.status, e)\n")
     out = _run_with_env(bad, KVX_LOG="9")
     assert out.stdout.startswith(f"{kvx.KVX_ERR_INVALID_ARG} ") and "KVX_LOG" in out.stdout
+
+
+# ---- kvx_select_launch: the launch a batch gets, decided on the host ----------
+
+def _batch(n, size, slot=None, src_phase=0, base_src=1 << 32, base_dst=1 << 36):
+    slot = slot or size
+    i = np.arange(n, dtype=np.uint64)
+    return (np.uint64(base_src + src_phase) + i * np.uint64(slot), np.uint64(base_dst) + i * np.uint64(slot),
+            np.full(n, size, dtype=np.uint64))
+
+
+def test_select_launch_kv_burst_and_tiny():
+    l = kvx.kvx_select_launch(*_batch(16384, 4096), None, "h2d")
+    assert (l["variant"], l["cta_budget"], l["threads"], l["unroll"]) == (kvx.KVX_VARIANT_LDG, 64, 256, 8)
+    assert l["assign"] == kvx.KVX_ASSIGN_DYNAMIC  # 16,384 units over 512 warps
+    l = kvx.kvx_select_launch(*_batch(1024, 4096), None, "d2h")
+    assert l["assign"] == kvx.KVX_ASSIGN_STATIC  # 2 units a warp: by position
+    assert l["stages"] == 0  # not used by LDG
+    l = kvx.kvx_select_launch(*_batch(3, 4096), None, "h2d")
+    assert l["cta_budget"] == 1  # the grid never exceeds the work
+    assert kvx.kvx_select_launch([], [], [], None, "h2d")["cta_budget"] == 0
+
+
+def test_select_launch_d2d_rows_follow_payload_and_alignment():
+    # 16 KiB chunks: the bulk ring from 256 MiB up, when 16-byte aligned
+    big = kvx.kvx_select_launch(*_batch(16384, 16384), None, "d2d")
+    assert (big["variant"], big["cta_budget"], big["stages"], big["threads"]) == (kvx.KVX_VARIANT_BULK, 456, 6, 0)
+    below = kvx.kvx_select_launch(*_batch(16383, 16384), None, "d2d")
+    assert below["variant"] == kvx.KVX_VARIANT_LDG and below["threads"] == 256
+    odd = kvx.kvx_select_launch(*_batch(16384, 16384, slot=32768, src_phase=8), None, "d2d")
+    assert odd["variant"] == kvx.KVX_VARIANT_LDG
+    # 9 % of the bytes misaligned still takes the ring; 11 % does not
+    s, d, z = _batch(20000, 16384, slot=32768)
+    s[:1800] += 8
+    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_BULK
+    s[:2200] = s[:2200] | 8
+    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    # small chunks stay with LDG at any payload
+    assert kvx.kvx_select_launch(*_batch(65536, 4096), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    # an explicit request wins over the table
+    forced = kvx.kvx_select_launch(*_batch(64, 16384, slot=32768, src_phase=8), None, "d2d", {"variant": "bulk"})
+    assert forced["variant"] == kvx.KVX_VARIANT_BULK
+    forced = kvx.kvx_select_launch(*_batch(16384, 4096), None, "h2d", {"assign": "static", "cta_budget": 7})
+    assert forced["assign"] == kvx.KVX_ASSIGN_STATIC and forced["cta_budget"] == 7
+
+
+def test_select_launch_rejects_what_copy_batch_rejects():
+    s, d, z = _batch(4, 4096)
+    z[2] = 12
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_select_launch(s, d, z, None, "h2d")
+    assert e.value.status == kvx.KVX_ERR_ALIGN
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_select_launch(*_batch(4, 4096), None, 9)
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+
+
+def test_select_launch_with_table_file_payload_rows(tmp_path):
+    table = tmp_path / "rows.table"
+    table.write_text("d2d inf ldg 77 128 4 3 0 static 2147483648\n")  # batches of 2 GiB and more
+    code = ("import numpy as np\n"
+            "from expert_host_block_gb300 import kvx\n"
+            "for n in (2, 1):\n"
+            "    s = np.uint64(1 << 32) + np.arange(n, dtype=np.uint64) * np.uint64(1 << 31)\n"
+            "    d = np.uint64(1 << 40) + np.arange(n, dtype=np.uint64) * np.uint64(1 << 31)\n"
+            "    z = np.full(n, 1 << 30, dtype=np.uint64)\n"
+            "    print(kvx.kvx_select_launch(s, d, z, None, 'd2d'))\n")
+    out = _run_with_env(code, KVX_TABLE=str(table))
+    lines = out.stdout.strip().splitlines()
+    assert "'cta_budget': 77, 'threads': 128, 'unroll': 4" in lines[0], out.stderr
+    assert "'variant': 2, 'cta_budget': 456" in lines[1]  # 1 GiB: the file row does not apply
