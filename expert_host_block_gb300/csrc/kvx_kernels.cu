@@ -1,19 +1,23 @@
 // Copy kernels of kvx for sm_103a.
 //
-// Both variants walk the same device-resident table of 32-byte chunk records
-// ({src, dst, len <= 16 KiB, desc}) as a persistent grid: work unit u goes to
-// worker (u mod workers), where a worker is a warp (LDG, whose units are warp
-// passes of at most 512 * U bytes) or a CTA (BULK, whose units are chunks).
-// Units are small and of nearly equal size, so handing them out round-robin
-// spreads the batch's bytes evenly over the workers, whatever mix of
-// descriptor sizes it holds (FreeToken issue #751, §Problem in upstream today
-// and §What we changed: split the call's bytes, not its banks, over the CTAs).
+// Both variants walk the same table of 32-byte chunk records ({src, dst,
+// len <= 16 KiB, desc}, after a header record) as a persistent grid: work
+// unit u goes to worker (u mod workers), where a worker is a warp (LDG, whose
+// units are warp passes of at most 512 * U bytes) or a CTA (BULK, whose units
+// are chunks). Units are small and of nearly equal size, so handing them out
+// round-robin spreads the batch's bytes evenly over the workers, whatever mix
+// of descriptor sizes it holds (FreeToken issue #751, §Problem in upstream
+// today and §What we changed: split the call's bytes, not its banks, over the
+// CTAs). Over the host link, where equal bytes do not take equal time, the
+// LDG kernel can instead hand units out from a counter (see the LDG variant).
 //
 // LDG variant: every lane moves 16-byte words, `U` loads in flight per lane
 // before the matching stores (the pages' LDG kernel keeps one 16-byte load in
-// flight per thread; FreeToken issue #751, §Problem in upstream today). A warp
-// reads the records of its next 32 chunks with one load per lane and passes
-// them around with shuffles, so no lane waits on a record load per chunk.
+// flight per thread; FreeToken issue #751, §Problem in upstream today). By
+// position, a warp reads the records of its next 32 chunks with one load per
+// lane and passes them around with shuffles, so no lane waits on a record
+// load per chunk; from the counter, lane 0 fetches the next unit's record
+// while the current one copies.
 //
 // BULK variant: one warp per CTA; lane 0 streams chunks through a ring of
 // shared::cta stages with cp.async.bulk loads completed on an mbarrier, then
