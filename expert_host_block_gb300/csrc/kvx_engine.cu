@@ -10,7 +10,9 @@
 //      records into a pinned staging slot (the reused pinned descriptor
 //      buffers of the vLLM PR #42212 report, §实现拆解 item 3 and §评论区精华:
 //      an unpinned buffer makes the "asynchronous" upload synchronous);
-//   3. one cudaMemcpyAsync of the table to the slot's device buffer;
+//   3. one cudaMemcpyAsync of the table to the slot's device buffer (on a
+//      side stream when the caller's stream still has work queued), or none
+//      for a small host-link batch, whose table the kernel reads in place;
 //   4. one launch of the persistent copy kernel with min(cta_budget, work)
 //      CTAs;
 //   5. record the slot's event and return: enqueue-only (PegaFlow issue #408,
