@@ -283,18 +283,19 @@ kvx_status check_kinds(const uint64_t *src, const uint64_t *dst, const uint64_t 
     return KVX_OK;
 }
 
-// Validate; count chunks and payload bytes, find the longest chunk, and count
+// Validate; count chunks and payload bytes, find the longest chunk, count
 // the bytes of descriptors whose source, destination and size are all
-// multiples of 16 (the bulk copy's condition).
+// multiples of 16 (the bulk copy's condition), and OR together the phases
+// (src ^ dst) mod 16 of the non-empty descriptors (0: every chunk matched).
 kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
                     int dir, int level, uint64_t *n_chunks, uint64_t *payload,
-                    uint32_t *max_chunk = nullptr, uint64_t *aligned16 = nullptr)
+                    uint32_t *max_chunk = nullptr, uint64_t *aligned16 = nullptr, uint64_t *phases = nullptr)
 {
     if (dir < KVX_H2D || dir > KVX_D2D)
         return fail(KVX_ERR_INVALID_ARG, "dir %d is not KVX_H2D, KVX_D2H or KVX_D2D", dir);
     if (level < 0 || level > 2)
         return fail(KVX_ERR_INVALID_ARG, "validation level %d is not 0, 1 or 2", level);
-    uint64_t chunks = 0, bytes = 0, longest = 0, aligned = 0;
+    uint64_t chunks = 0, bytes = 0, longest = 0, aligned = 0, phase = 0;
     if (n) {
         if (!src || !dst || !sizes)
             return fail(KVX_ERR_INVALID_ARG, "null descriptor array with n = %zu", n);
@@ -311,6 +312,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
             chunks += (z >> 14) + ((z & (KVX_CHUNK_BYTES - 1)) != 0);
             bytes += z;
             aligned += ((s | d | z) & 15u) ? 0 : z;
+            phase |= live & (s ^ d) & 15u;
             longest = z > longest ? z : longest;
         }
         if (!bad) {
@@ -318,7 +320,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
                 return fail(KVX_ERR_CAPACITY, "batch needs more than KVX_MAX_CHUNKS (%u) chunks",
                             KVX_MAX_CHUNKS);
         } else {
-            chunks = bytes = longest = aligned = 0;
+            chunks = bytes = longest = aligned = phase = 0;
         }
         for (size_t i = 0; bad && i < n; ++i) {
             const uint64_t z = sizes[i];
@@ -339,6 +341,7 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
             chunks += chunks_of(z);
             bytes += z;
             aligned += ((s | d | z) & 15u) ? 0 : z;
+            phase |= (s ^ d) & 15u;
             if (z > longest)
                 longest = z;
             if (chunks > KVX_MAX_CHUNKS)
@@ -364,6 +367,8 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
         *max_chunk = (uint32_t)std::min<uint64_t>(longest, KVX_CHUNK_BYTES);
     if (aligned16)
         *aligned16 = aligned;
+    if (phases)
+        *phases = phase;
     return KVX_OK;
 }
 
@@ -393,13 +398,13 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
 // check or is longer than one chunk; the caller then takes the exact two-pass
 // path, which also reports the first failing descriptor.
 struct PackAcc {
-    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0;
+    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0, phase = 0;
 };
 
 void pack_fast_range(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t a, size_t b,
                      kvx_chunk *out, PackAcc &acc)
 {
-    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0;
+    uint64_t bad = 0, bytes = 0, longest = 0, aligned = 0, phase = 0;
     for (size_t i = a; i < b; ++i) {
         const uint64_t z = sizes[i], s = src[i], d = dst[i];
         const uint64_t live = z ? ~0ull : 0ull;
@@ -407,6 +412,7 @@ void pack_fast_range(const uint64_t *src, const uint64_t *dst, const uint64_t *s
         bad |= (uint64_t)(z > KVX_CHUNK_BYTES) << 4;
         bytes += z;
         aligned += ((s | d | z) & 15u) ? 0 : z;
+        phase |= live & (s ^ d) & 15u;
         longest = z > longest ? z : longest;
         out[i] = kvx_chunk{s, d, (uint32_t)z, (uint32_t)i, 0};
     }
@@ -414,10 +420,12 @@ void pack_fast_range(const uint64_t *src, const uint64_t *dst, const uint64_t *s
     acc.bytes = bytes;
     acc.longest = longest;
     acc.aligned = aligned;
+    acc.phase = phase;
 }
 
 bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
-               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk, uint64_t *aligned16)
+               kvx_chunk *out, uint64_t *n_chunks, uint64_t *payload, uint32_t *max_chunk, uint64_t *aligned16,
+               uint64_t *phases)
 {
     // Large batches are split over the calling thread and the worker pool.
     constexpr size_t kParallelMin = 8192, kMinPart = 4096;
@@ -440,6 +448,7 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
         t.bytes += acc[p].bytes;
         t.longest = std::max(t.longest, acc[p].longest);
         t.aligned += acc[p].aligned;
+        t.phase |= acc[p].phase;
     }
     if (t.bad || n > KVX_MAX_CHUNKS)
         return false;
@@ -447,6 +456,7 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
     *payload = t.bytes;
     *max_chunk = (uint32_t)t.longest;
     *aligned16 = t.aligned;
+    *phases = t.phase;
     return true;
 }
 
@@ -480,17 +490,19 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 //
 // D2D, from the mean of 30 L2-flushed launches per shape (the event timer
 // ticks in ~1 us, so medians of short launches are coarse): the bulk ring is
-// fastest for batches of 256 MiB and more in chunks of 12 KiB and more (16 KiB
-// x 32,768: 0.990 of HBM with 456 CTAs and 96 KiB rings, against 0.963 for
-// LDG), and LDG with 256-thread CTAs for everything else (16 KiB x 4,096:
-// 0.970 against 0.894 for the ring, whose fill and drain do not amortise over
-// 64 MiB; 4 KiB x 65,536: 0.958 against 0.935 for 512-thread CTAs).
+// fastest for batches of 256 MiB and more of full 16 KiB chunks (16 KiB x
+// 32,768: 0.992 of HBM with 456 CTAs and 96 KiB rings, against 0.985 for LDG;
+// 64 KiB x 8,192: 0.996 against 0.985), and LDG for everything else, with
+// 1,216 CTAs of 128 threads (about two waves of the SMs): 4 KiB x 65,536
+// 0.971, 24 KiB x 21,845 (chunks of 16 and 8 KiB, which waste the ring's
+// stages) 0.974 against 0.934 for the ring, 16 KiB x 4,096 0.981 against
+// 0.894 for the ring, whose fill and drain do not amortise over 64 MiB.
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
-    {KVX_D2D, 12287, {KVX_VARIANT_LDG, 608, 256, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 608, 256, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 
 int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
@@ -500,6 +512,7 @@ struct BatchShape {
     uint64_t mean_chunk = 0;        // payload / chunks
     uint64_t payload = ~0ull;       // bytes (unknown: as large as can be)
     bool aligned = true;            // may take a BULK row
+    bool matched = false;           // every chunk's src and dst agree mod 16 (unknown: no)
 };
 
 bool row_matches(const TableRow &r, int dir, const BatchShape &b)
@@ -527,12 +540,13 @@ kvx_launch table_launch(int dir, const BatchShape &b)
 
 // The shape of a validated batch: whether it is aligned enough for a BULK row
 // (see the table), its mean chunk and its payload.
-BatchShape batch_shape(uint64_t chunks, uint64_t payload, uint64_t aligned16)
+BatchShape batch_shape(uint64_t chunks, uint64_t payload, uint64_t aligned16, uint64_t phases)
 {
     BatchShape b;
     b.mean_chunk = chunks ? payload / chunks : 0;
     b.payload = payload;
     b.aligned = aligned16 / 9 >= payload / 10;  // at least ~90 % (no overflow near 2^64)
+    b.matched = phases == 0;
     return b;
 }
 
@@ -573,6 +587,7 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     out->stages = stages;
     out->store_policy = policy;
     out->assign = assign;
+    out->matched = shape.matched;
     return KVX_OK;
 }
 
@@ -830,7 +845,8 @@ kvx_status bits_status(unsigned bits)
         return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
     if (bits)
         return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s", bits,
-                    (bits & kvx::kDevErrBadRecord) ? " chunk record longer than KVX_CHUNK_BYTES;" : "",
+                    (bits & kvx::kDevErrBadRecord) ? " inconsistent chunk record (longer than KVX_CHUNK_BYTES, or "
+                                                     "src and dst out of phase in a phase-matched launch);" : "",
                     (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
                     (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
     return KVX_OK;
@@ -860,12 +876,13 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     Slot *s = nullptr;
     if (ring_acquire(dev, n, &s) != KVX_OK)
         return KVX_OK;
-    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
     Launch l;
-    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk, &aligned16) ||
+    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk, &aligned16,
+                   &phases) ||
         payload == 0 ||
-        resolve(dir, batch_shape(chunks, payload, aligned16), want, &l) != KVX_OK) {
+        resolve(dir, batch_shape(chunks, payload, aligned16, phases), want, &l) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;
     }
@@ -899,6 +916,7 @@ struct kvx_desc_buf {
     uint64_t payload = 0;
     int dir = KVX_H2D;
     kvx_launch selected{};
+    bool matched = false;  // every uploaded chunk's src and dst agree mod 16
 };
 
 struct kvx_devlist {
@@ -990,13 +1008,13 @@ kvx_status kvx_select_launch(const uint64_t *src, const uint64_t *dst, const uin
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
-    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, 0, &chunks, &payload, &max_chunk, &aligned16);
+    st = validate(src, dst, sizes, n, dir, 0, &chunks, &payload, &max_chunk, &aligned16, &phases);
     if (st != KVX_OK)
         return st;
     Launch l;
-    st = resolve(dir, batch_shape(chunks, payload, aligned16), want, &l);
+    st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), want, &l);
     if (st != KVX_OK)
         return st;
     const bool ldg = l.variant == KVX_VARIANT_LDG;
@@ -1025,13 +1043,13 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
         if (done)
             return st;
     }
-    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16, &phases);
     if (st != KVX_OK)
         return st;
     Launch l;
-    st = resolve(dir, batch_shape(chunks, payload, aligned16), want, &l);
+    st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), want, &l);
     if (st != KVX_OK)
         return st;
     if (chunks == 0)
@@ -1110,16 +1128,16 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
-    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16, &phases);
     if (st != KVX_OK)
         return st;
     if (chunks > b->cap)
         return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, buffer holds %zu",
                     (unsigned long long)chunks, b->cap);
     Launch l;
-    st = resolve(dir, batch_shape(chunks, payload, aligned16), nullptr, &l);
+    st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), nullptr, &l);
     if (st != KVX_OK)
         return st;
     bool cap = false;
@@ -1144,6 +1162,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     b->payload = payload;
     b->dir = dir;
     b->selected = {l.variant, l.ctas, l.threads, l.unroll, l.stages, l.store_policy, l.assign};
+    b->matched = l.matched;
     return KVX_OK;
 }
 
@@ -1179,6 +1198,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     st = resolve(b->dir, BatchShape{}, &merged, &l);
     if (st != KVX_OK)
         return st;
+    l.matched = b->matched;
     if (b->n_chunks == 0)
         return KVX_OK;
     bool cap = false;
@@ -1589,9 +1609,9 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
-    uint64_t chunks = 0, payload = 0, aligned16 = 0;
+    uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
-    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16);
+    st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16, &phases);
     if (st != KVX_OK)
         return st;
     if (chunks > KVX_NOALLOC_MAX_CHUNKS)
@@ -1601,7 +1621,7 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_launch want{};
     want.cta_budget = cta_budget;
     Launch l;
-    st = resolve(dir, batch_shape(chunks, payload, aligned16), &want, &l);
+    st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), &want, &l);
     if (st != KVX_OK)
         return st;
     if (chunks == 0)

@@ -14,7 +14,7 @@ namespace kvx {
 // Bits of the device status word (one per device, shared by all streams).
 enum : unsigned {
     kDevErrTimeout = 1u,    // a bounded mbarrier wait gave up
-    kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES
+    kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES, or out of phase for its launch
     kDevErrCount = 4u,      // a device-side descriptor count above the list's capacity (clamped)
     kDevErrBadDesc = 8u,    // a device-side descriptor failed validation (skipped)
 };
@@ -38,6 +38,7 @@ struct Launch {
     int stages;        // BULK ring size in units of KVX_CHUNK_BYTES
     int store_policy;  // LDG store cache policy
     int assign;        // LDG: KVX_ASSIGN_STATIC or KVX_ASSIGN_DYNAMIC
+    bool matched;      // LDG: every chunk's src and dst agree mod 16 (decided from the packed batch)
 };
 
 // Every device chunk table starts with one header record that holds the

@@ -406,7 +406,9 @@ def test_select_launch_d2d_rows_follow_payload_and_alignment():
     big = kvx.kvx_select_launch(*_batch(16384, 16384), None, "d2d")
     assert (big["variant"], big["cta_budget"], big["stages"], big["threads"]) == (kvx.KVX_VARIANT_BULK, 456, 6, 0)
     below = kvx.kvx_select_launch(*_batch(16383, 16384), None, "d2d")
-    assert below["variant"] == kvx.KVX_VARIANT_LDG and below["threads"] == 256
+    assert below["variant"] == kvx.KVX_VARIANT_LDG and below["threads"] == 128
+    # chunks of 16 and 8 KiB (mean 12 KiB) stay with LDG at any payload
+    assert kvx.kvx_select_launch(*_batch(16384, 24576), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
     odd = kvx.kvx_select_launch(*_batch(16384, 16384, slot=32768, src_phase=8), None, "d2d")
     assert odd["variant"] == kvx.KVX_VARIANT_LDG
     # 9 % of the bytes misaligned still takes the ring; 11 % does not
