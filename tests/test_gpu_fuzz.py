@@ -28,8 +28,8 @@ def _cuda():
     torch.cuda.set_device(0)
 
 
-def _random_case(seed):
-    g = np.random.default_rng([W.SEED, 77, seed])
+def _random_case(seed, matched=False):
+    g = np.random.default_rng([W.SEED, 77 if not matched else 78, seed])
     direction = ["h2d", "d2h", "d2d"][seed % 3]
     n = int(g.choice([1, 3, 17, 200, 1500, 5000]))
     kind = g.integers(0, 4, n)
@@ -37,8 +37,11 @@ def _random_case(seed):
     sizes[g.random(n) < 0.03] = 0
     slot = 104 * 1024
     n_slots = 2 * n + 4
-    dst = (g.permutation(n_slots)[:n] * slot + 8 * g.integers(0, 2, n)).astype(np.uint64)
-    src = (g.integers(0, n_slots, n) * slot + 8 * g.integers(0, 2, n)).astype(np.uint64)  # may repeat
+    dst_phase = 8 * g.integers(0, 2, n)
+    # matched: every descriptor's src and dst agree mod 16 (the phase-matched kernel instance)
+    src_phase = dst_phase if matched else 8 * g.integers(0, 2, n)
+    dst = (g.permutation(n_slots)[:n] * slot + dst_phase).astype(np.uint64)
+    src = (g.integers(0, n_slots, n) * slot + src_phase).astype(np.uint64)  # may repeat
     body = n_slots * slot
     launch = {"variant": str(g.choice(["ldg", "bulk"])), "cta_budget": int(g.choice([1, 3, 16, 64, 300]))}
     if launch["variant"] == "ldg":
@@ -56,6 +59,20 @@ def _random_case(seed):
 @pytest.mark.parametrize("seed", range(36))
 def test_random_batches(seed):
     specs, b, launch = _random_case(seed)
+    p = Pools(specs)
+    try:
+        want = p.expected([b])
+        run_batch(p, b, launch=launch)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_phase_matched_batches(seed):
+    # heads and tails of 8 bytes, but src and dst in phase: the kernel without re-pairing
+    specs, b, launch = _random_case(seed, matched=True)
     p = Pools(specs)
     try:
         want = p.expected([b])
