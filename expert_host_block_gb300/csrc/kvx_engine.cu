@@ -1332,6 +1332,8 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
             merged.unroll = want->unroll;
         if (want->store_policy)
             merged.store_policy = want->store_policy;
+        if (want->assign)
+            merged.assign = want->assign;
     }
     merged.variant = KVX_VARIANT_LDG;
     Launch lc;

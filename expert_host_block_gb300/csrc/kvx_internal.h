@@ -24,6 +24,7 @@ struct DevListMeta {
     uint64_t total;      // chunks of the valid descriptors
     uint32_t n;          // descriptors taken (the count, clamped to the capacity)
     uint32_t max_chunk;  // longest chunk, bytes
+    unsigned long long next;  // the copy kernel's unit counter (zeroed by the plan kernel)
 };
 
 // Bounded-wait limit of the bulk kernel's mbarrier waits (ns of %globaltimer).

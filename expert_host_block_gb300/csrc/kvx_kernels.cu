@@ -695,6 +695,7 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
         meta->total = s_carry;
         meta->n = n;
         meta->max_chunk = s_max;
+        meta->next = 0;
         if (s_bad)
             atomicOr(&g_status, kDevErrBadDesc);
     }
@@ -702,11 +703,48 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
 
 constexpr uint32_t kSmemOffsets = 4096;  // scans of up to 4,095 descriptors are searched in shared memory
 
+// The record of unit u of a device list: pass u / total of chunk u % total,
+// the chunk found by binary search over the scan (offsets[lo] <= c <
+// offsets[lo + 1], offsets[0] = 0, offsets[n] = total).
+__device__ __forceinline__ Rec devlist_rec(uint64_t u, uint64_t total, uint32_t n, uint32_t unit,
+                                           const uint64_t *s_off, bool in_smem,
+                                           const uint64_t *__restrict__ offsets,
+                                           const uint64_t *__restrict__ src, const uint64_t *__restrict__ dst,
+                                           const uint64_t *__restrict__ sizes, uint32_t *pass_out)
+{
+    const uint64_t pass = u / total;
+    const uint64_t c = u - pass * total;
+    uint32_t lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        const uint64_t o = in_smem ? s_off[mid] : __ldg(offsets + mid);
+        if (o <= c)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const uint64_t j = c - (in_smem ? s_off[lo] : __ldg(offsets + lo));
+    const uint64_t z = sizes[lo], off = j * KVX_CHUNK_BYTES;
+    Rec r;
+    r.s = src[lo] + off;
+    r.d = dst[lo] + off;
+    r.l = (uint32_t)(z - off < KVX_CHUNK_BYTES ? z - off : KVX_CHUNK_BYTES);
+    if (pass * unit >= r.l)
+        r.l = 0;
+    *pass_out = (uint32_t)pass;
+    return r;
+}
+
+// Units by position, or (dynamic, with at least kDynamicMinUnitsPerWarp units
+// a warp) warp w takes unit w and then one unit at a time from meta->next,
+// with the next unit's record on its way while the current one copies, as in
+// the LDG kernel. The plan kernel zeroes the counter before every copy, so a
+// replayed graph needs no reset.
 template <int U, int P>
 __global__ void __launch_bounds__(512) kvx_copy_devlist_kernel(
     const uint64_t *__restrict__ src, const uint64_t *__restrict__ dst,
-    const uint64_t *__restrict__ sizes, const DevListMeta *__restrict__ meta,
-    const uint64_t *__restrict__ offsets)
+    const uint64_t *__restrict__ sizes, DevListMeta *__restrict__ meta,
+    const uint64_t *__restrict__ offsets, bool dynamic)
 {
     __shared__ uint64_t s_off[kSmemOffsets];
     const uint64_t total = meta->total;
@@ -726,39 +764,50 @@ __global__ void __launch_bounds__(512) kvx_copy_devlist_kernel(
     const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
     const uint64_t n_units = total * passes;
-    for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
-        const uint64_t mine = base + (uint64_t)lane * nwarps;
-        Rec r = {0, 0, 0};
-        uint32_t k = 0;
-        if (mine < n_units) {
-            const uint64_t pass = mine / total;
-            const uint64_t c = mine - pass * total;
-            k = (uint32_t)pass;
-            // offsets[lo] <= c < offsets[hi], with offsets[0] = 0 and offsets[n] = total
-            uint32_t lo = 0, hi = n;
-            while (hi - lo > 1) {
-                const uint32_t mid = (lo + hi) >> 1;
-                const uint64_t o = in_smem ? s_off[mid] : __ldg(offsets + mid);
-                if (o <= c)
-                    lo = mid;
-                else
-                    hi = mid;
+    if (!dynamic || n_units < kDynamicMinUnitsPerWarp * nwarps) {
+        for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
+            const uint64_t mine = base + (uint64_t)lane * nwarps;
+            Rec r = {0, 0, 0};
+            uint32_t k = 0;
+            if (mine < n_units)
+                r = devlist_rec(mine, total, n, unit, s_off, in_smem, offsets, src, dst, sizes, &k);
+            const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
+            for (int jj = 0; jj < cnt; ++jj) {
+                const Rec cc = shfl_rec(r, jj);
+                const uint32_t kk = __shfl_sync(kFull, k, jj);
+                if (cc.l)
+                    copy_pass<U, P>(cc.s, cc.d, cc.l, kk, lane);
             }
-            const uint64_t j = c - (in_smem ? s_off[lo] : __ldg(offsets + lo));
-            const uint64_t z = sizes[lo], off = j * KVX_CHUNK_BYTES;
-            r.s = src[lo] + off;
-            r.d = dst[lo] + off;
-            r.l = (uint32_t)(z - off < KVX_CHUNK_BYTES ? z - off : KVX_CHUNK_BYTES);
-            if ((uint64_t)k * unit >= r.l)
-                r.l = 0;
         }
-        const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
-        for (int jj = 0; jj < cnt; ++jj) {
-            const Rec cc = shfl_rec(r, jj);
-            const uint32_t kk = __shfl_sync(kFull, k, jj);
-            if (cc.l)
-                copy_pass<U, P>(cc.s, cc.d, cc.l, kk, lane);
+        return;
+    }
+    unsigned long long *ctr = &meta->next;
+    uint64_t cur = gwarp;
+    unsigned long long nx = 0;
+    Rec rc = {0, 0, 0};
+    uint32_t kc = 0;
+    if (lane == 0) {
+        nx = nwarps + atomicAdd(ctr, 1ull);
+        if (cur < n_units)
+            rc = devlist_rec(cur, total, n, unit, s_off, in_smem, offsets, src, dst, sizes, &kc);
+    }
+    while (cur < n_units) {
+        unsigned long long nn = 0;
+        Rec rn = {0, 0, 0};
+        uint32_t kn = 0;
+        if (lane == 0) {
+            nn = nwarps + atomicAdd(ctr, 1ull);
+            if (nx < n_units)
+                rn = devlist_rec(nx, total, n, unit, s_off, in_smem, offsets, src, dst, sizes, &kn);
         }
+        const Rec c = shfl_rec(rc, 0);
+        const uint32_t kk = __shfl_sync(kFull, kc, 0);
+        if (c.l)
+            copy_pass<U, P>(c.s, c.d, c.l, kk, lane);
+        cur = __shfl_sync(kFull, nx, 0);
+        nx = nn;
+        rc = rn;
+        kc = kn;
     }
 }
 
@@ -827,13 +876,13 @@ cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n
 
 template <int U>
 cudaError_t launch_devlist_p(int p, int ctas, int threads, const uint64_t *src, const uint64_t *dst,
-                            const uint64_t *sizes, const DevListMeta *meta, const uint64_t *offsets,
+                            const uint64_t *sizes, DevListMeta *meta, const uint64_t *offsets, bool dyn,
                             cudaStream_t s)
 {
     switch (p) {
-    case 1: kvx_copy_devlist_kernel<U, 1><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
-    case 2: kvx_copy_devlist_kernel<U, 2><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
-    default: kvx_copy_devlist_kernel<U, 0><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets); break;
+    case 1: kvx_copy_devlist_kernel<U, 1><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
+    case 2: kvx_copy_devlist_kernel<U, 2><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
+    default: kvx_copy_devlist_kernel<U, 0><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
     }
     return cudaGetLastError();
 }
@@ -902,10 +951,11 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
+    const bool dyn = l.assign == KVX_ASSIGN_DYNAMIC;
     switch (l.unroll) {
-    case 2: return launch_devlist_p<2>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
-    case 4: return launch_devlist_p<4>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
-    default: return launch_devlist_p<8>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, stream);
+    case 2: return launch_devlist_p<2>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
+    case 4: return launch_devlist_p<4>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
+    default: return launch_devlist_p<8>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
     }
 }
 

@@ -59,18 +59,27 @@ def test_moe_calls_from_device_lists():
 
 @pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
 @pytest.mark.parametrize("odd", [False, True])
-def test_sweep_cells_from_device_lists(direction, odd):
+@pytest.mark.parametrize("assign", ["static", "dynamic"])
+def test_sweep_cells_from_device_lists(direction, odd, assign):
     w = W.sweep_cell(24, 1500, direction, odd_tails=odd)
     (b,) = w.batches
     p = Pools(w.pools)
     lst = kvx.DeviceList(8192)
     arr = DevArrays(8192)
     try:
-        want = p.expected([b])
-        arr.fill(*p.addrs(b))
-        lst.copy(*arr.ptrs(), direction, launch={"cta_budget": 13, "unroll": 4})
-        kvx.kvx_stream_check(None)
-        p.assert_equal(want)
+        # twice over the same list: the plan kernel re-zeroes the unit counter
+        for _ in range(2):
+            dstbuf = p.bufs["dst"]
+            if isinstance(dstbuf, kvx.HostBuffer):
+                dstbuf.numpy()[:] = W.CANARY
+            else:
+                dstbuf.fill_(W.CANARY)
+            torch.cuda.synchronize()
+            want = p.expected([b])
+            arr.fill(*p.addrs(b))
+            lst.copy(*arr.ptrs(), direction, launch={"cta_budget": 13, "unroll": 4, "assign": assign})
+            kvx.kvx_stream_check(None)
+            p.assert_equal(want)
     finally:
         lst.close()
         p.close()
