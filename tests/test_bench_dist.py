@@ -91,3 +91,11 @@ def test_clock_sampler_without_nvml_reports_why():
         assert s["samples"] == 0 and "NVML" in s["note"]
     else:  # a machine with a GPU
         assert s["samples"] >= 2
+
+
+def test_parse_cell_specs():
+    assert bench.parse_cell("h2d:4:65536") == ("h2d", 4, 65536, False)
+    assert bench.parse_cell("d2d:28:4096:odd") == ("d2d", 28, 4096, True)
+    for bad in ("x2y:4:16", "h2d:4", "h2d:4:16:even", "d2h:4:16:odd:1"):
+        with pytest.raises(SystemExit):
+            bench.parse_cell(bad)
