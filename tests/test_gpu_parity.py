@@ -96,6 +96,39 @@ def test_kv_burst_bidirectional(launch):
         p.close()
 
 
+def test_kv_burst_as_bench_times_it():
+    """The bench's timed loop, full size: 8 rotating sets of resident tables (kvx_copy_uploaded with the
+    table's launch: LDG, units from the counter), the two halves of each burst joined, 12 bursts."""
+    import bench
+    w = W.kv_burst(n_sets=8)
+    p = Pools(w.pools)
+    bufs = []
+    try:
+        batches = [b for pair in w.batches for b in pair]
+        want = p.expected(batches)
+        s_h, s_d = torch.cuda.Stream(), torch.cuda.Stream()
+        for h2d, d2h in w.batches:
+            bh, bd = kvx.DescBuf(h2d.n), kvx.DescBuf(d2h.n)
+            bh.upload(*p.addrs(h2d), "h2d", s_h)
+            bd.upload(*p.addrs(d2h), "d2h", s_d)
+            bufs.append((bh, bd))
+        assert bufs[0][0].info()[2]["assign"] == kvx.KVX_ASSIGN_DYNAMIC
+        join = bench.BurstJoin(torch, s_h, s_d)
+        for k in range(12):
+            bh, bd = bufs[k % 8]
+            bh.copy(stream=s_h)
+            bd.copy(stream=s_d)
+            join()
+        kvx.kvx_stream_check(s_h)
+        kvx.kvx_stream_check(s_d)
+        p.assert_equal(want)
+    finally:
+        for bh, bd in bufs:
+            bh.close()
+            bd.close()
+        p.close()
+
+
 def test_kv_burst_many_sets_ring_reuse():
     """More calls than staging slots, on two streams: every slot is reused."""
     w = W.kv_burst(n_sets=12, n_per_dir=2048, pool_bytes=256 * W.MIB)
