@@ -755,19 +755,30 @@ cudaError_t aux_stream(int dev, AuxKind kind, cudaStream_t *out)
 // Upload a packed chunk table from its pinned slot to the slot's device table,
 // ordered before whatever is enqueued on `stream` next. ring_acquire returned
 // the slot only after the last kernel reading its device table finished, so
-// the upload depends on nothing already on `stream`. When `stream` is idle it
-// goes on `stream`; when work is still queued there (a transfer worker that
-// submits the next burst while the previous one copies) it goes on the upload
-// side stream and `stream` waits for it, so the upload overlaps that work
-// instead of idling the link between two copy kernels.
-cudaError_t upload_table(int dev, Slot *s, size_t bytes, cudaStream_t stream)
+// the upload depends on nothing already on `stream`. When `stream` is idle
+// (`busy` false) it goes on `stream`; when work is still queued there (a
+// transfer worker that submits the next burst while the previous one copies)
+// it goes on the upload side stream and `stream` waits for it, so the upload
+// overlaps that work instead of idling the link between two copy kernels.
+// Whether `stream` still has work queued (cudaErrorNotReady, cleared); other
+// errors are returned in *err.
+bool stream_busy(cudaStream_t stream, cudaError_t *err)
 {
-    cudaError_t q = cudaStreamQuery(stream);
-    if (q == cudaSuccess)
+    const cudaError_t q = cudaStreamQuery(stream);
+    *err = cudaSuccess;
+    if (q == cudaErrorNotReady) {
+        cudaGetLastError();  // not sticky; clear it
+        return true;
+    }
+    if (q != cudaSuccess)
+        *err = q;
+    return false;
+}
+
+cudaError_t upload_table(int dev, Slot *s, size_t bytes, cudaStream_t stream, bool busy)
+{
+    if (!busy)
         return cudaMemcpyAsync(s->dev, s->host, bytes, cudaMemcpyHostToDevice, stream);
-    if (q != cudaErrorNotReady)
-        return q;
-    cudaGetLastError();  // cudaErrorNotReady is not sticky; clear it
     cudaStream_t side = nullptr;
     cudaError_t e = aux_stream(dev, kAuxUpload, &side);
     if (e == cudaSuccess && !s->uploaded)
@@ -781,19 +792,23 @@ cudaError_t upload_table(int dev, Slot *s, size_t bytes, cudaStream_t stream)
     return e;
 }
 
-// Small host-link batches skip the table upload: the kernel reads its records
-// from the pinned staging slot itself (a unified address), which takes a
-// copy-engine operation and its latency off every call (1,024 x 4 KiB H2D,
-// submit + copy + status read: 67 -> 72 GB/s). Only for launches that assign
-// units by position (the work counter must stay in device memory) and for at
-// most kInPlaceMaxChunks records: a warp then reads its records once, where
-// a long launch over a busy link would wait on each 32-record batch. D2D keeps
-// the upload: its records would cross the host link for nothing.
+// Small batches skip the table upload: the kernel reads its records from the
+// pinned staging slot itself (a unified address), which takes a copy-engine
+// operation and its latency off the call (1,024 x 4 KiB H2D, submit + copy +
+// status read: 67 -> 72 GB/s; 256 x 4 KiB D2D: 41.7 -> 36.4 us). Only for
+// launches that assign units by position (the work counter must stay in
+// device memory) and for at most kInPlaceMaxChunks records: a warp then reads
+// its records once, where a long launch over a busy link would wait on each
+// 32-record batch. A D2D batch does it only when the caller's stream is idle:
+// when it is busy, the upload overlaps that work on the side stream and the
+// kernel then reads its records from HBM, a shorter round trip than the host
+// link's (256 x 4 KiB: 6.5 against 7.4 us).
 constexpr uint64_t kInPlaceMaxChunks = 4096;
 
-bool table_in_place(int dir, const kvx::Launch &l, uint64_t chunks, uint32_t max_chunk)
+bool table_in_place(int dir, const kvx::Launch &l, uint64_t chunks, uint32_t max_chunk, bool busy)
 {
-    return dir != KVX_D2D && chunks <= kInPlaceMaxChunks && !kvx::ldg_dynamic(l, (uint32_t)chunks, max_chunk);
+    return (dir != KVX_D2D || !busy) && chunks <= kInPlaceMaxChunks &&
+           !kvx::ldg_dynamic(l, (uint32_t)chunks, max_chunk);
 }
 
 void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
@@ -810,9 +825,16 @@ void ring_release(int dev, Slot *s, cudaStream_t stream, bool record)
 kvx_status launch_from_slot(int dev, Slot *s, int dir, const kvx::Launch &l, uint64_t chunks,
                             uint32_t max_chunk, cudaStream_t stream)
 {
+    cudaError_t qe = cudaSuccess;
+    const bool busy = stream_busy(stream, &qe);
+    if (qe != cudaSuccess) {
+        ring_release(dev, s, stream, false);
+        return cuda_fail(qe, "cudaStreamQuery");
+    }
     kvx_chunk *table = s->host_dev;
-    if (!table_in_place(dir, l, chunks, max_chunk)) {
-        cudaError_t e = upload_table(dev, s, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk), stream);
+    if (!table_in_place(dir, l, chunks, max_chunk, busy)) {
+        cudaError_t e =
+            upload_table(dev, s, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk), stream, busy);
         if (e != cudaSuccess) {
             ring_release(dev, s, stream, false);
             return cuda_fail(e, "chunk table upload");

@@ -15,8 +15,8 @@
  * How kvx runs a batch. The host validates the descriptors, cuts each one
  * into chunks of at most KVX_CHUNK_BYTES at 8-byte granularity, packs the
  * 32-byte chunk records into a pinned staging buffer, uploads the table with
- * one cudaMemcpyAsync (small host-link tables are read by the kernel in
- * place instead) and launches one persistent copy kernel on `stream` with at
+ * one cudaMemcpyAsync (small tables are read by the kernel in place
+ * instead) and launches one persistent copy kernel on `stream` with at
  * most `cta_budget` CTAs. Every call is enqueue-only: it returns once the
  * work is queued (PegaFlow issue #408, follow-up §2: the transfer backend
  * contract is enqueue-only and never synchronises).
@@ -143,13 +143,13 @@ typedef struct kvx_desc_buf kvx_desc_buf;
  * ring has 8 slots per device; a call takes the most recently used slot whose
  * copy has finished, and waits on the host only when none has (then for the
  * least recently used one). A slot allocates on first use and grows, once, for
- * a batch bigger than it holds. A host-link (H2D, D2H) batch of at most
- * 4,096 chunks whose units the kernel assigns by position is not uploaded:
- * the kernel reads its records from the mapped staging slot. Otherwise, when
- * `stream` still has work queued, the table upload runs on a library side
- * stream (overlapping that work) and the copy kernel waits for it on
- * `stream`. The copy stays ordered after all earlier work on `stream` either
- * way. */
+ * a batch bigger than it holds. A batch of at most 4,096 chunks whose units
+ * the kernel assigns by position is not uploaded (for D2D: only when `stream`
+ * is idle): the kernel reads its records from the mapped staging slot.
+ * Otherwise, when `stream` still has work queued, the table upload runs on a
+ * library side stream (overlapping that work) and the copy kernel waits for
+ * it on `stream`. The copy stays ordered after all earlier work on `stream`
+ * either way. */
 kvx_status kvx_copy_batch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                           const uint64_t *sizes, size_t n, int dir, int cta_budget,
                           void *stream);
