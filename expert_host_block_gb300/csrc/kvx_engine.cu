@@ -372,12 +372,13 @@ kvx_status validate(const uint64_t *src, const uint64_t *dst, const uint64_t *si
     return KVX_OK;
 }
 
-// Pack the chunk records of a validated batch. Chunk k of a descriptor covers
-// bytes [k * 16 KiB, min((k + 1) * 16 KiB, size)).
-size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n, kvx_chunk *out)
+// Pack the chunk records of descriptors [a, b) of a validated batch from out[0].
+// Chunk k of a descriptor covers bytes [k * 16 KiB, min((k + 1) * 16 KiB, size)).
+size_t pack_range(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t a, size_t b,
+                  kvx_chunk *out)
 {
     size_t m = 0;
-    for (size_t i = 0; i < n; ++i) {
+    for (size_t i = a; i < b; ++i) {
         const uint64_t z = sizes[i];
         for (uint64_t o = 0; o < z; o += KVX_CHUNK_BYTES) {
             kvx_chunk &c = out[m++];
@@ -389,6 +390,38 @@ size_t pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, siz
         }
     }
     return m;
+}
+
+// Pack a validated batch that expands to `chunks` records. A large table is
+// split over the caller and the worker pool by descriptor ranges, each written
+// at its own offset: the copy cannot start before the table is packed. Waking
+// sleeping pool threads costs about 20 us on Grace, so only tables of 32 Ki
+// records and more (1 MiB, ~100 us for one thread) are split: a MoE call's
+// 3,552 records packed in 22 us alone and 40 us split, the pool asleep after
+// the previous call's wait.
+void pack(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n, kvx_chunk *out,
+          uint64_t chunks = 0)
+{
+    constexpr uint64_t kParallelMinChunks = 32768;
+    constexpr int kMaxParts = 16;
+    kvx::Workers &w = kvx::Workers::get();
+    const int parts = std::min<int>({w.threads() + 1, kMaxParts, (int)std::min<size_t>(n, kMaxParts)});
+    if (chunks >= kParallelMinChunks && parts > 1) {
+        size_t lo[kMaxParts + 1];
+        uint64_t off[kMaxParts + 1];
+        off[0] = 0;
+        for (int p = 0; p <= parts; ++p)
+            lo[p] = n * (size_t)p / (size_t)parts;
+        for (int p = 0; p < parts; ++p) {
+            uint64_t c = 0;
+            for (size_t i = lo[p]; i < lo[p + 1]; ++i)
+                c += chunks_of(sizes[i]);
+            off[p + 1] = off[p] + c;
+        }
+        if (w.run(parts, [&](int p) { pack_range(src, dst, sizes, lo[p], lo[p + 1], out + off[p]); }))
+            return;
+    }
+    pack_range(src, dst, sizes, 0, n, out);
 }
 
 // Validation level 0 and packing in one pass, for the common batch of many
@@ -1006,7 +1039,7 @@ kvx_status kvx_plan_chunks(const uint64_t *src, const uint64_t *dst, const uint6
     if (chunks > max_out)
         return fail(KVX_ERR_CAPACITY, "batch needs %llu chunks, output holds %zu",
                     (unsigned long long)chunks, max_out);
-    pack(src, dst, sizes, n, out);
+    pack(src, dst, sizes, n, out, chunks);
     return KVX_OK;
 }
 
@@ -1089,7 +1122,7 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     st = ring_acquire(dev, (size_t)chunks, &s);
     if (st != KVX_OK)
         return st;
-    pack(src, dst, sizes, n, s->host + kvx::kTableHeader);
+    pack(src, dst, sizes, n, s->host + kvx::kTableHeader, chunks);
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
     return launch_from_slot(dev, s, dir, l, chunks, max_chunk, stream);
 }
@@ -1173,7 +1206,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
         KVX_CUDA_TRY(cudaEventSynchronize(b->upload_done));
         b->upload_recorded = false;
     }
-    pack(src, dst, sizes, n, b->host + kvx::kTableHeader);
+    pack(src, dst, sizes, n, b->host + kvx::kTableHeader, chunks);
     if (chunks)
         KVX_CUDA_TRY(cudaMemcpyAsync(b->dev, b->host, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                      cudaMemcpyHostToDevice, stream));
@@ -1662,7 +1695,7 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
             return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk table)");
         g_noalloc_dev[dev] = static_cast<kvx_chunk *>(p);
     }
-    pack(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader);
+    pack(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader, chunks);
     KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage,
                                  (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                  cudaMemcpyHostToDevice, stream));

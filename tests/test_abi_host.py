@@ -91,6 +91,26 @@ def test_chunk_table_moves_the_same_bytes(seed):
     assert np.array_equal(got, want)
 
 
+def test_parallel_pack_matches_single_thread(tmp_path):
+    """A table of >= 32,768 records is packed by the worker pool in descriptor ranges; it must equal the
+    single-threaded table record for record."""
+    code = ("import numpy as np\n"
+            "from expert_host_block_gb300 import kvx\n"
+            "g = np.random.default_rng(5)\n"
+            "n = 16000\n"
+            "z = (8 * g.integers(0, 80 * 1024 // 8, n)).astype(np.uint64)\n"
+            "s = np.uint64(1 << 40) + np.arange(n, dtype=np.uint64) * np.uint64(1 << 20) + np.uint64(8) * g.integers(0, 2, n).astype(np.uint64)\n"
+            "d = np.uint64(1 << 41) + np.arange(n, dtype=np.uint64) * np.uint64(1 << 20)\n"
+            "t = kvx.kvx_plan_chunks(s, d, z)\n"
+            f"np.save(r'{tmp_path}/' + __import__('os').environ['KVX_PACK_THREADS'] + '.npy', t.view(np.uint8))\n"
+            "print(t.size)\n")
+    a = _run_with_env(code, KVX_PACK_THREADS="0")
+    b = _run_with_env(code, KVX_PACK_THREADS="3")
+    assert a.returncode == 0 and b.returncode == 0, a.stderr + b.stderr
+    assert int(a.stdout) >= 32768 and a.stdout == b.stdout
+    assert np.array_equal(np.load(tmp_path / "0.npy"), np.load(tmp_path / "3.npy"))
+
+
 def test_moe_chunk_count_closed_form(golden):
     """1 MiB / 16 KiB + 128 KiB / 16 KiB + 1 + 512 KiB / 16 KiB + ceil(68 KiB / 16 KiB) + 1 = 111."""
     rows = [int(x) for x in golden("moe_banks.txt")["row_bytes"]]
