@@ -646,6 +646,51 @@ kvx_status is_capturing(cudaStream_t stream, bool *cap)
 // ---------------------------------------------------------------------------
 constexpr int kRingSlots = 8;
 constexpr int kMaxDevices = 64;
+
+// Device error flags: kvx::kErrWords words per device in one page of host
+// memory, registered with the driver as mapped pinned memory on first use (a
+// static array, so no allocation), written by kernels with plain stores and
+// read and cleared here by atomic exchanges once the work that may have set
+// them has completed.
+alignas(4096) unsigned g_err_words[kMaxDevices][16];
+static_assert(kvx::kErrWords <= 16, "error flag words per device");
+struct ErrMap {
+    std::mutex mu;
+    bool registered = false;
+    unsigned *dev[kMaxDevices] = {};  // device address of each device's words
+};
+ErrMap g_err_map;
+
+// The device address of `dev`'s error flags (`dev` current in this thread).
+// Registers the page on the first call in the process: call it outside
+// stream capture (object creation and uncapturable entry points do).
+kvx_status err_flags(int dev, unsigned **out)
+{
+    std::lock_guard<std::mutex> g(g_err_map.mu);
+    if (!g_err_map.registered) {
+        KVX_CUDA_TRY(cudaHostRegister(g_err_words, sizeof(g_err_words),
+                                      cudaHostRegisterMapped | cudaHostRegisterPortable));
+        g_err_map.registered = true;
+    }
+    if (!g_err_map.dev[dev]) {
+        void *p = nullptr;
+        KVX_CUDA_TRY(cudaHostGetDevicePointer(&p, g_err_words[dev], 0));
+        g_err_map.dev[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_err_map.dev[dev];
+    return KVX_OK;
+}
+
+// Read and clear `dev`'s error flags as a kDevErr* bit set.
+unsigned take_err(int dev)
+{
+    unsigned bits = 0;
+    for (int i = 0; i < kvx::kErrWords; ++i)
+        if (__atomic_exchange_n(&g_err_words[dev][i], 0u, __ATOMIC_ACQ_REL))
+            bits |= 1u << i;
+    return bits;
+}
+
 constexpr size_t kMinSlotChunks = 1 << 16;
 
 struct Slot {
@@ -756,10 +801,9 @@ kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
     return KVX_OK;
 }
 
-// Side streams of each device: one for chunk-table uploads, one for status
-// reads. Created on first use with the device's highest priority, never
-// destroyed.
-enum AuxKind { kAuxUpload = 0, kAuxStatus = 1, kAuxKinds = 2 };
+// Side streams of each device (one, for chunk-table uploads). Created on first
+// use with the device's highest priority, never destroyed.
+enum AuxKind { kAuxUpload = 0, kAuxKinds = 1 };
 struct AuxStreams {
     std::mutex mu;
     cudaStream_t s[kAuxKinds] = {};
@@ -874,24 +918,29 @@ kvx_status launch_from_slot(int dev, Slot *s, int dir, const kvx::Launch &l, uin
         }
         table = s->dev;
     }
-    cudaError_t e = kvx::launch_copy(l, table, (uint32_t)chunks, max_chunk, stream);
+    unsigned *err = nullptr;
+    kvx_status est = err_flags(dev, &err);
+    if (est != KVX_OK) {
+        ring_release(dev, s, stream, false);
+        return est;
+    }
+    cudaError_t e = kvx::launch_copy(l, table, (uint32_t)chunks, max_chunk, err, stream);
     ring_release(dev, s, stream, true);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     return KVX_OK;
 }
 
-// mapped pinned words for kvx_stream_check
-constexpr unsigned kStatusWords = 1024;
-struct StatusWords {
+// Status tokens: an event recorded on the caller's stream, per device a ring
+// of kStatusEvents with a generation count each.
+constexpr unsigned kStatusEvents = 1024;
+struct StatusEvents {
     std::mutex mu;
-    unsigned *words = nullptr;  // mapped pinned, written by the fetch kernel
-    cudaEvent_t marks[kStatusWords] = {};   // the caller's stream reached the read
-    cudaEvent_t events[kStatusWords] = {};  // the read has run
-    uint64_t gen[kStatusWords] = {};
+    cudaEvent_t events[kStatusEvents] = {};
+    uint64_t gen[kStatusEvents] = {};
     unsigned next = 0;
 };
-StatusWords g_status_words[kMaxDevices];
+StatusEvents g_status_events[kMaxDevices];
 
 // The status a word of status bits stands for (kvx_stream_check's answer).
 kvx_status bits_status(unsigned bits)
@@ -972,10 +1021,12 @@ struct kvx_desc_buf {
     int dir = KVX_H2D;
     kvx_launch selected{};
     bool matched = false;  // every uploaded chunk's src and dst agree mod 16
+    unsigned *err = nullptr;  // the device's error flags
 };
 
 struct kvx_devlist {
     int device = 0;
+    unsigned *err = nullptr;  // the device's error flags
     uint32_t max_n = 0;
     kvx::DevListMeta *meta = nullptr;  // 256 bytes, then the offsets
     uint64_t *offsets = nullptr;
@@ -1148,6 +1199,17 @@ kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
     if (!b)
         return fail(KVX_ERR_CAPACITY, "out of host memory");
     cudaError_t e = cudaGetDevice(&b->device);
+    if (e == cudaSuccess && (b->device < 0 || b->device >= kMaxDevices)) {
+        delete b;
+        return fail(KVX_ERR_INVALID_ARG, "device out of range");
+    }
+    if (e == cudaSuccess) {
+        const kvx_status est = err_flags(b->device, &b->err);
+        if (est != KVX_OK) {
+            delete b;
+            return est;
+        }
+    }
     const size_t bytes = (max_chunks + kvx::kTableHeader) * sizeof(kvx_chunk);
     if (e == cudaSuccess)
         e = cudaMalloc(reinterpret_cast<void **>(&b->dev), bytes);
@@ -1266,7 +1328,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     // come back for a new one)
     if (!cap && b->use_recorded)
         KVX_CUDA_TRY(cudaStreamWaitEvent(stream, b->last_use, 0));
-    cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, stream);
+    cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, b->err, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     if (!cap) {
@@ -1327,6 +1389,17 @@ kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out)
         return fail(KVX_ERR_CAPACITY, "out of host memory");
     l->max_n = max_n;
     cudaError_t e = cudaGetDevice(&l->device);
+    if (e == cudaSuccess && (l->device < 0 || l->device >= kMaxDevices)) {
+        delete l;
+        return fail(KVX_ERR_INVALID_ARG, "device out of range");
+    }
+    if (e == cudaSuccess) {
+        const kvx_status est = err_flags(l->device, &l->err);
+        if (est != KVX_OK) {
+            delete l;
+            return est;
+        }
+    }
     if (e == cudaSuccess)
         e = cudaMalloc(reinterpret_cast<void **>(&l->meta),
                        256 + ((size_t)max_n + 1) * sizeof(uint64_t));
@@ -1399,7 +1472,7 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
-    cudaError_t e = kvx::launch_devlist(lc, src, dst, sizes, count, l->max_n, l->meta, l->offsets, stream);
+    cudaError_t e = kvx::launch_devlist(lc, src, dst, sizes, count, l->max_n, l->meta, l->offsets, l->err, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "device-list launch");
     if (!cap) {
@@ -1409,73 +1482,48 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     return KVX_OK;
 }
 
-namespace {
-
-// Queue a read of the status word behind the work on `stream`. With `side`
-// (and outside a capture) the read runs on the status side stream, so later
-// work on `stream` does not wait for it; otherwise it is a launch on `stream`,
-// which reaches the host sooner when the caller waits for it at once.
-kvx_status status_enqueue(cudaStream_t stream, kvx_status_token *tok, bool side)
+kvx_status kvx_status_enqueue(void *stream_, kvx_status_token *tok)
 {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!tok)
         return fail(KVX_ERR_INVALID_ARG, "null token");
     int dev = 0;
     KVX_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices)
         return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
-    StatusWords &w = g_status_words[dev];
-    std::lock_guard<std::mutex> g(w.mu);
-    if (!w.words)
-        KVX_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void **>(&w.words), kStatusWords * sizeof(unsigned),
-                                   cudaHostAllocMapped | cudaHostAllocPortable));
     bool cap = false;
     kvx_status st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
-    const unsigned slot = w.next++ % kStatusWords;
+    if (cap)
+        return fail(KVX_ERR_CAPTURE, "a status read waits on the host; enqueue it on the stream that replays the graph");
+    unsigned *err = nullptr;
+    st = err_flags(dev, &err);  // registers the flags before any kernel could need them
+    if (st != KVX_OK)
+        return st;
+    StatusEvents &w = g_status_events[dev];
+    std::lock_guard<std::mutex> g(w.mu);
+    const unsigned slot = w.next++ % kStatusEvents;
     if (!w.events[slot])
         KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.events[slot], cudaEventDisableTiming));
-    if (!w.marks[slot])
-        KVX_CUDA_TRY(cudaEventCreateWithFlags(&w.marks[slot], cudaEventDisableTiming));
-    w.words[slot] = 0;
-    if (cap || !side) {
-        // inside a capture the read becomes a node of the graph
-        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, stream));
-        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
-    } else {
-        // the read waits for the work already on `stream`, on a side stream,
-        // so that the next copy on `stream` does not wait for the read
-        cudaStream_t aux = nullptr;
-        KVX_CUDA_TRY(aux_stream(dev, kAuxStatus, &aux));
-        KVX_CUDA_TRY(cudaEventRecord(w.marks[slot], stream));
-        KVX_CUDA_TRY(cudaStreamWaitEvent(aux, w.marks[slot], 0));
-        KVX_CUDA_TRY(kvx::launch_status_fetch(w.words + slot, aux));
-        KVX_CUDA_TRY(cudaEventRecord(w.events[slot], aux));
-    }
+    KVX_CUDA_TRY(cudaEventRecord(w.events[slot], stream));
     tok->slot = slot;
     tok->gen = ++w.gen[slot];
     tok->device = dev;
     return KVX_OK;
 }
 
-}  // namespace
-
-kvx_status kvx_status_enqueue(void *stream, kvx_status_token *tok)
-{
-    return status_enqueue(static_cast<cudaStream_t>(stream), tok, true);
-}
-
 namespace {
 
-kvx_status token_slot(const kvx_status_token *tok, StatusWords **w)
+kvx_status token_event(const kvx_status_token *tok, cudaEvent_t *ev)
 {
-    if (!tok || tok->device < 0 || tok->device >= kMaxDevices || tok->slot >= kStatusWords)
+    if (!tok || tok->device < 0 || tok->device >= kMaxDevices || tok->slot >= kStatusEvents)
         return fail(KVX_ERR_INVALID_ARG, "not a status token");
-    StatusWords &sw = g_status_words[tok->device];
+    StatusEvents &sw = g_status_events[tok->device];
     std::lock_guard<std::mutex> g(sw.mu);
-    if (!sw.words || sw.gen[tok->slot] != tok->gen)
-        return fail(KVX_ERR_INVALID_ARG, "status token expired: %u later reads reused its slot", kStatusWords);
-    *w = &sw;
+    if (!sw.events[tok->slot] || sw.gen[tok->slot] != tok->gen)
+        return fail(KVX_ERR_INVALID_ARG, "status token expired: %u later reads reused its slot", kStatusEvents);
+    *ev = sw.events[tok->slot];
     return KVX_OK;
 }
 
@@ -1486,11 +1534,11 @@ kvx_status kvx_status_query(const kvx_status_token *tok, int *ready)
     if (!ready)
         return fail(KVX_ERR_INVALID_ARG, "null output");
     *ready = 0;
-    StatusWords *w = nullptr;
-    kvx_status st = token_slot(tok, &w);
+    cudaEvent_t ev = nullptr;
+    kvx_status st = token_event(tok, &ev);
     if (st != KVX_OK)
         return st;
-    const cudaError_t e = cudaEventQuery(w->events[tok->slot]);
+    const cudaError_t e = cudaEventQuery(ev);
     if (e == cudaErrorNotReady) {
         cudaGetLastError();
         return KVX_OK;
@@ -1498,26 +1546,31 @@ kvx_status kvx_status_query(const kvx_status_token *tok, int *ready)
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaEventQuery(status read)");
     *ready = 1;
-    return bits_status(*reinterpret_cast<volatile unsigned *>(w->words + tok->slot));
+    return bits_status(take_err(tok->device));
 }
 
 kvx_status kvx_status_wait(const kvx_status_token *tok)
 {
-    StatusWords *w = nullptr;
-    kvx_status st = token_slot(tok, &w);
+    cudaEvent_t ev = nullptr;
+    kvx_status st = token_event(tok, &ev);
     if (st != KVX_OK)
         return st;
-    KVX_CUDA_TRY(cudaEventSynchronize(w->events[tok->slot]));
-    return bits_status(*reinterpret_cast<volatile unsigned *>(w->words + tok->slot));
+    KVX_CUDA_TRY(cudaEventSynchronize(ev));
+    return bits_status(take_err(tok->device));
 }
 
 kvx_status kvx_stream_check(void *stream)
 {
-    kvx_status_token tok;
-    kvx_status st = status_enqueue(static_cast<cudaStream_t>(stream), &tok, false);
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
+    unsigned *err = nullptr;
+    kvx_status st = err_flags(dev, &err);
     if (st != KVX_OK)
         return st;
-    return kvx_status_wait(&tok);
+    KVX_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    return bits_status(take_err(dev));
 }
 
 kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_t *free_bytes,
@@ -1624,7 +1677,15 @@ kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
     if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull)
         return fail(KVX_ERR_INVALID_ARG, "timeout_ns %llu not in [1 ms, 10 s]",
                     (unsigned long long)timeout_ns);
-    KVX_CUDA_TRY(kvx::launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream)));
+    int dev = 0;
+    KVX_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
+    unsigned *err = nullptr;
+    kvx_status st = err_flags(dev, &err);
+    if (st != KVX_OK)
+        return st;
+    KVX_CUDA_TRY(kvx::launch_wait_selftest(timeout_ns, err, static_cast<cudaStream_t>(stream)));
     return KVX_OK;
 }
 
@@ -1651,8 +1712,11 @@ std::mutex g_noalloc_mu;
 
 // Device address of g_noalloc_table per device. In host code the symbol is
 // only a host-side stand-in, so the address comes from cudaGetSymbolAddress
-// with the device current (first call on each device).
+// with the device current (first call on each device). The same first call
+// maps the library's error flags if no other call did (a registration of a
+// static host page, not an allocation).
 kvx_chunk *g_noalloc_dev[kMaxDevices];
+unsigned *g_noalloc_err[kMaxDevices];
 
 }  // namespace
 
@@ -1693,13 +1757,16 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_table);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk table)");
+        const kvx_status est = err_flags(dev, &g_noalloc_err[dev]);
+        if (est != KVX_OK)
+            return est;
         g_noalloc_dev[dev] = static_cast<kvx_chunk *>(p);
     }
     pack(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader, chunks);
     KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage,
                                  (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                  cudaMemcpyHostToDevice, stream));
-    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, max_chunk, stream);
+    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, max_chunk, g_noalloc_err[dev], stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     return KVX_OK;

@@ -11,13 +11,16 @@ static_assert(sizeof(kvx_chunk) == 32, "chunk records are 32 bytes");
 
 namespace kvx {
 
-// Bits of the device status word (one per device, shared by all streams).
+// Kinds of device error. Each is reported in its own flag word (kind bit b ->
+// word b) of a device's kErrWords mapped pinned words, shared by all streams
+// of the device; the host reads them as a bit set.
 enum : unsigned {
     kDevErrTimeout = 1u,    // a bounded mbarrier wait gave up
     kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES, or out of phase for its launch
     kDevErrCount = 4u,      // a device-side descriptor count above the list's capacity (clamped)
     kDevErrBadDesc = 8u,    // a device-side descriptor failed validation (skipped)
 };
+constexpr int kErrWords = 4;
 
 // Result of the device-list plan kernel, read by the device-list copy kernel.
 struct DevListMeta {
@@ -64,24 +67,21 @@ bool ldg_dynamic(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len);
 // its header record, n_chunks records follow. max_chunk_len is the longest
 // record's len (it sets the LDG kernel's passes per chunk).
 cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
-                        uint32_t max_chunk_len, cudaStream_t stream);
+                        uint32_t max_chunk_len, unsigned *err, cudaStream_t stream);
 
 // Enqueue the plan and copy kernels over a device-resident descriptor list:
 // count and arrays in device memory, meta and offsets[max_n + 1] scratch.
 // l.ctas is used as is (the work is not known on the host).
 cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t *dst,
                            const uint64_t *sizes, const uint32_t *count, uint32_t max_n,
-                           DevListMeta *meta, uint64_t *offsets, cudaStream_t stream);
+                           DevListMeta *meta, uint64_t *offsets, unsigned *err, cudaStream_t stream);
 
-// Enqueue a 1-thread kernel that moves the status word into *host_word
-// (mapped pinned) and clears it.
-cudaError_t launch_status_fetch(unsigned *host_word, cudaStream_t stream);
 
 // Set the calling thread's kvx_last_error() message and return `status`.
 kvx_status set_error(kvx_status status, const char *message);
 
 // Enqueue the bounded-wait self-test kernel.
-cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned *err, cudaStream_t stream);
 
 // Shared memory of a bulk ring of `units` x KVX_CHUNK_BYTES.
 size_t bulk_smem_bytes(int units);

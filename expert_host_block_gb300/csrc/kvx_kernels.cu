@@ -38,9 +38,16 @@
 
 namespace kvx {
 
-__device__ unsigned g_status;
-
 namespace {
+
+// Device errors: one flag word per kind (kDevErr* bit b -> word b) in mapped
+// pinned host memory, set by a plain store. The host reads and clears the
+// words once the stream or event it waits for has completed, so no atomic
+// and no extra kernel is needed to report them.
+__device__ __forceinline__ void report(unsigned *err, unsigned kind)
+{
+    *reinterpret_cast<volatile unsigned *>(err + (__ffs(kind) - 1)) = 1u;
+}
 
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -232,7 +239,7 @@ struct Rec {
     uint32_t l;
 };
 
-__device__ __forceinline__ Rec load_rec(const kvx_chunk *__restrict__ tab, uint64_t c)
+__device__ __forceinline__ Rec load_rec(const kvx_chunk *__restrict__ tab, uint64_t c, unsigned *err)
 {
     const uint4 *p = reinterpret_cast<const uint4 *>(tab + c);
     const uint4 a = __ldg(p);
@@ -242,7 +249,7 @@ __device__ __forceinline__ Rec load_rec(const kvx_chunk *__restrict__ tab, uint6
     r.d = (uint64_t)a.z | ((uint64_t)a.w << 32);
     r.l = b.x;
     if (r.l > KVX_CHUNK_BYTES) {  // never produced by the host planner
-        atomicOr(&g_status, kDevErrBadRecord);
+        report(err, kDevErrBadRecord);
         r.l = 0;
     }
     return r;
@@ -283,20 +290,20 @@ __device__ __forceinline__ Rec shfl_rec(const Rec &r, int src_lane)
 // mismatched record means a bad table: reported and skipped, never copied with
 // misaligned 16-byte accesses.
 template <bool M>
-__device__ __forceinline__ bool phase_ok(const Rec &c, uint32_t lane)
+__device__ __forceinline__ bool phase_ok(const Rec &c, uint32_t lane, unsigned *err)
 {
     if (!M || ((c.s ^ c.d) & 15u) == 0)
         return true;
     if (lane == 0)
-        atomicOr(&g_status, kDevErrBadRecord);
+        report(err, kDevErrBadRecord);
     return false;
 }
 
 __device__ __forceinline__ Rec unit_rec(const kvx_chunk *__restrict__ tab, uint64_t u, uint32_t n_chunks,
-                                        uint32_t pass_bytes, uint32_t *pass_out)
+                                        uint32_t pass_bytes, uint32_t *pass_out, unsigned *err)
 {
     const uint64_t pass = u / n_chunks;
-    Rec r = load_rec(tab, u - pass * n_chunks);
+    Rec r = load_rec(tab, u - pass * n_chunks, err);
     if (pass * pass_bytes >= r.l)
         r.l = 0;  // this chunk has no such pass
     *pass_out = (uint32_t)pass;
@@ -306,7 +313,7 @@ __device__ __forceinline__ Rec unit_rec(const kvx_chunk *__restrict__ tab, uint6
 template <int U, int P, bool M>
 __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
                                                             uint32_t n_chunks, uint32_t passes,
-                                                            unsigned long long *ctr)
+                                                            unsigned long long *ctr, unsigned *err)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t wpb = blockDim.x >> 5;
@@ -319,12 +326,12 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
             Rec r = {0, 0, 0};
             uint32_t k = 0;
             if (mine < n_units)
-                r = unit_rec(tab, mine, n_chunks, PassBytes<U>::value, &k);
+                r = unit_rec(tab, mine, n_chunks, PassBytes<U>::value, &k, err);
             const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
             for (int j = 0; j < cnt; ++j) {
                 const Rec c = shfl_rec(r, j);
                 const uint32_t kk = __shfl_sync(kFull, k, j);
-                if (c.l && phase_ok<M>(c, lane))
+                if (c.l && phase_ok<M>(c, lane, err))
                     copy_pass<U, P, M>(c.s, c.d, c.l, kk, lane);
             }
         }
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
     if (lane == 0) {
         nx = nwarps + atomicAdd(&ctr[0], 1ull);
         if (cur < n_units)
-            rc = unit_rec(tab, cur, n_chunks, PassBytes<U>::value, &kc);
+            rc = unit_rec(tab, cur, n_chunks, PassBytes<U>::value, &kc, err);
     }
     while (cur < n_units) {
         unsigned long long nn = 0;
@@ -347,11 +354,11 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
         if (lane == 0) {
             nn = nwarps + atomicAdd(&ctr[0], 1ull);
             if (nx < n_units)
-                rn = unit_rec(tab, nx, n_chunks, PassBytes<U>::value, &kn);
+                rn = unit_rec(tab, nx, n_chunks, PassBytes<U>::value, &kn, err);
         }
         const Rec c = shfl_rec(rc, 0);
         const uint32_t kk = __shfl_sync(kFull, kc, 0);
-        if (c.l && phase_ok<M>(c, lane))
+        if (c.l && phase_ok<M>(c, lane, err))
             copy_pass<U, P, M>(c.s, c.d, c.l, kk, lane);
         cur = __shfl_sync(kFull, nx, 0);
         nx = nn;
@@ -497,7 +504,7 @@ constexpr int kBulkMaxStages = 32;
 // commits back.
 __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__restrict__ tab,
                                                            uint32_t n_chunks, uint32_t stage,
-                                                           uint32_t S, uint64_t wait_ns)
+                                                           uint32_t S, uint64_t wait_ns, unsigned *err)
 {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t bars[kBulkMaxStages];
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     auto load_batch = [&](uint64_t k0) {
         Rec r = {0, 0, 0};
         if (k0 + lane < my_n)
-            r = load_rec(tab, (uint64_t)blockIdx.x + (k0 + lane) * gridDim.x);
+            r = load_rec(tab, (uint64_t)blockIdx.x + (k0 + lane) * gridDim.x, err);
         const uint32_t slot = (uint32_t)((k0 + lane) & 63u);
         w_src[slot] = r.s;
         w_dst[slot] = r.d;
@@ -599,7 +606,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
 
     if (timed_out) {
         if (lane == 0)
-            atomicOr(&g_status, kDevErrTimeout);
+            report(err, kDevErrTimeout);
         // Let the loads still in flight land before the shared memory goes away.
         if (lane == 0)
             for (uint32_t s = 0; s < S; ++s)
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
 __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
     const uint64_t *__restrict__ src, const uint64_t *__restrict__ dst,
     const uint64_t *__restrict__ sizes, const uint32_t *__restrict__ count, uint32_t max_n,
-    DevListMeta *__restrict__ meta, uint64_t *__restrict__ offsets)
+    DevListMeta *__restrict__ meta, uint64_t *__restrict__ offsets, unsigned *err)
 {
     __shared__ uint64_t warp_sums[32];
     __shared__ uint64_t s_carry;
@@ -636,7 +643,7 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
     uint32_t n = *count;
     if (n > max_n) {
         if (tid == 0)
-            atomicOr(&g_status, kDevErrCount);
+            report(err, kDevErrCount);
         n = max_n;
     }
     if (tid == 0) {
@@ -697,7 +704,7 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
         meta->max_chunk = s_max;
         meta->next = 0;
         if (s_bad)
-            atomicOr(&g_status, kDevErrBadDesc);
+            report(err, kDevErrBadDesc);
     }
 }
 
@@ -811,15 +818,9 @@ __global__ void __launch_bounds__(512) kvx_copy_devlist_kernel(
     }
 }
 
-// ---- status word and the bounded-wait self-test ---------------------------
+// ---- the bounded-wait self-test -------------------------------------------
 
-__global__ void kvx_status_fetch_kernel(unsigned *host_word)
-{
-    *host_word = atomicExch(&g_status, 0u);
-    __threadfence_system();
-}
-
-__global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns)
+__global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns, unsigned *err)
 {
     __shared__ __align__(8) uint64_t bar;
     const uint32_t b = smem_u32(&bar);
@@ -830,34 +831,34 @@ __global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns)
     __syncwarp();
     // Nothing arrives on the barrier, so phase 0 never completes.
     if (threadIdx.x == 0 && !mbar_wait_bounded(b, 0, timeout_ns))
-        atomicOr(&g_status, kDevErrTimeout);
+        report(err, kDevErrTimeout);
     __syncwarp();
 }
 
 template <int U, int P>
 cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
-                       unsigned long long *ctr, bool matched, cudaStream_t s)
+                       unsigned long long *ctr, bool matched, unsigned *err, cudaStream_t s)
 {
     if (matched)
-        kvx_copy_ldg_kernel<U, P, true><<<ctas, threads, 0, s>>>(t, n, passes, ctr);
+        kvx_copy_ldg_kernel<U, P, true><<<ctas, threads, 0, s>>>(t, n, passes, ctr, err);
     else
-        kvx_copy_ldg_kernel<U, P, false><<<ctas, threads, 0, s>>>(t, n, passes, ctr);
+        kvx_copy_ldg_kernel<U, P, false><<<ctas, threads, 0, s>>>(t, n, passes, ctr, err);
     return cudaGetLastError();
 }
 
 template <int U>
 cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint32_t n,
-                         uint32_t passes, unsigned long long *ctr, bool matched, cudaStream_t s)
+                         uint32_t passes, unsigned long long *ctr, bool matched, unsigned *err, cudaStream_t s)
 {
     switch (p) {
-    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, ctr, matched, s);
-    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, ctr, matched, s);
-    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, ctr, matched, s);
+    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, ctr, matched, err, s);
+    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, ctr, matched, err, s);
+    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, ctr, matched, err, s);
     }
 }
 
 cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n, uint32_t max_chunk_len,
-                        cudaStream_t s)
+                        unsigned *err, cudaStream_t s)
 {
     const uint32_t ring = (uint32_t)bulk_smem_bytes(ring_units);
     uint32_t stage = (max_chunk_len + 15u) & ~15u;
@@ -870,7 +871,7 @@ cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n
                                          (int)ring);
     if (e != cudaSuccess)
         return e;
-    kvx_copy_bulk_kernel<<<ctas, 32, ring, s>>>(t, n, stage, S, kBulkWaitNs);
+    kvx_copy_bulk_kernel<<<ctas, 32, ring, s>>>(t, n, stage, S, kBulkWaitNs, err);
     return cudaGetLastError();
 }
 
@@ -924,30 +925,30 @@ int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
 }
 
 cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
-                        uint32_t max_chunk_len, cudaStream_t stream)
+                        uint32_t max_chunk_len, unsigned *err, cudaStream_t stream)
 {
     if (n_chunks == 0)
         return cudaSuccess;
     const int ctas = work_ctas(l, n_chunks, max_chunk_len);
     const kvx_chunk *recs = table + kTableHeader;
     if (l.variant == KVX_VARIANT_BULK) {
-        return launch_bulk(ctas, l.stages, recs, n_chunks, max_chunk_len, stream);
+        return launch_bulk(ctas, l.stages, recs, n_chunks, max_chunk_len, err, stream);
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
     unsigned long long *ctr =
         ldg_dynamic(l, n_chunks, max_chunk_len) ? reinterpret_cast<unsigned long long *>(table) : nullptr;
     switch (l.unroll) {
-    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, stream);
-    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, stream);
-    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, stream);
+    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
+    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
+    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
     }
 }
 
 cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t *dst,
                            const uint64_t *sizes, const uint32_t *count, uint32_t max_n,
-                           DevListMeta *meta, uint64_t *offsets, cudaStream_t stream)
+                           DevListMeta *meta, uint64_t *offsets, unsigned *err, cudaStream_t stream)
 {
-    kvx_devlist_plan_kernel<<<1, 1024, 0, stream>>>(src, dst, sizes, count, max_n, meta, offsets);
+    kvx_devlist_plan_kernel<<<1, 1024, 0, stream>>>(src, dst, sizes, count, max_n, meta, offsets, err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -959,15 +960,10 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
     }
 }
 
-cudaError_t launch_status_fetch(unsigned *host_word, cudaStream_t stream)
-{
-    kvx_status_fetch_kernel<<<1, 1, 0, stream>>>(host_word);
-    return cudaGetLastError();
-}
 
-cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t stream)
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned *err, cudaStream_t stream)
 {
-    kvx_wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+    kvx_wait_selftest_kernel<<<1, 32, 0, stream>>>(timeout_ns, err);
     return cudaGetLastError();
 }
 

@@ -42,7 +42,7 @@ KVX_ERR_DEVICE_FAULT = 8
 KVX_ERR_CAPTURE = 9
 
 # the C ABI version this binding's structures follow (KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR)
-KVX_VERSION = 3
+KVX_VERSION = 4
 
 KVX_CHUNK_BYTES = 16384
 KVX_MAX_CHUNKS = 1 << 22
@@ -509,19 +509,19 @@ def kvx_stream_check(stream=None) -> None:
 
 
 def kvx_status_enqueue(stream=None) -> kvx_status_token:
-    """Queue a read of the device status word behind the work on `stream`; returns its token."""
+    """Mark the current end of `stream`'s work (an event); returns the token whose wait reads the device's errors."""
     tok = kvx_status_token()
     _check(_load().kvx_status_enqueue(_stream(stream), ctypes.byref(tok)))
     return tok
 
 
 def kvx_status_wait(tok: kvx_status_token) -> None:
-    """Block until the read ran; raises like kvx_stream_check."""
+    """Block until the stream reached the token, then read the device's errors; raises like kvx_stream_check."""
     _check(_load().kvx_status_wait(ctypes.byref(tok)))
 
 
 def kvx_status_query(tok: kvx_status_token) -> bool:
-    """True once the read ran (raising if it found an error); False while pending."""
+    """True once the stream reached the token (raising if the device reported an error); False while pending."""
     r = _int()
     _check(_load().kvx_status_query(ctypes.byref(tok), ctypes.byref(r)))
     return bool(r.value)

@@ -60,7 +60,7 @@ extern "C" {
 #endif
 
 #define KVX_VERSION_MAJOR 0
-#define KVX_VERSION_MINOR 3
+#define KVX_VERSION_MINOR 4
 
 /* Largest chunk a descriptor is cut into: 16 KiB, the chunk of the FreeToken
  * gather (FreeToken issue #751, §What we changed: "chunks of up to 16 KiB,
@@ -336,11 +336,15 @@ int kvx_version(void); /* KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR */
 
 /* ---- device status, memory ---------------------------------------------- */
 
-/* Synchronise `stream`, then read and clear the device status word that
- * kernels set when a bounded wait gives up. The word is shared by all
- * streams of the device, so an error raised by a kernel on another stream
- * may be reported here. KVX_OK, KVX_ERR_TIMEOUT, KVX_ERR_DEVICE_FAULT or
- * KVX_ERR_CUDA. */
+/* Synchronise `stream`, then read and clear the device's error flags, which
+ * kernels set (a bounded wait that gave up, an inconsistent chunk record, a
+ * device-list count above capacity or a bad device-list descriptor). The
+ * flags live in a page of mapped pinned host memory that kvx registers with
+ * the driver on its first use in the process (a static page, no allocation);
+ * kernels set them with plain stores, so reading them needs no kernel. They
+ * are shared by all streams of the device, so an error raised by a kernel on
+ * another stream may be reported here. KVX_OK, KVX_ERR_TIMEOUT,
+ * KVX_ERR_DEVICE_FAULT or KVX_ERR_CUDA. */
 kvx_status kvx_stream_check(void *stream);
 
 /* The current device's SM count, per-thread stack limit and free / total
@@ -356,17 +360,19 @@ kvx_status kvx_device_query(int *sm_count, size_t *stack_bytes_per_thread, size_
 /* The same read without blocking, for a transfer worker that submits the
  * next batch before collecting the previous one (the enqueue-only contract of
  * PegaFlow issue #408, follow-up §2: record completion, poll it later).
- * kvx_status_enqueue queues a read of the status word behind the work already
- * on `stream` and returns a token; kvx_status_wait blocks until that read has
- * run and returns what kvx_stream_check would have; kvx_status_query does not
- * block (*ready = 0 while the stream has not reached the read; otherwise
- * *ready = 1 and the status). Reading clears the word, and the word is shared
- * by all streams of the device. Outside a graph capture the read runs on a
- * library side stream once `stream` reaches it, so work enqueued on `stream`
- * after the token does not wait for the read (and an error that such work
- * raises may be reported by this token rather than the next). Inside a capture
- * the read is a node on `stream`. A token stays valid for the next 1,024 reads
- * enqueued on its device; after that, KVX_ERR_INVALID_ARG. */
+ * kvx_status_enqueue records an event behind the work already on `stream`
+ * and returns a token; nothing is added to the stream's work, so later work
+ * on `stream` does not wait for the read. kvx_status_wait blocks until the
+ * stream has reached the token, then reads and clears the device's error
+ * flags and returns what kvx_stream_check would have; kvx_status_query does
+ * not block (*ready = 0 while the stream has not reached the token;
+ * otherwise *ready = 1 and the status). The flags are shared by all streams
+ * of the device, so an error that work enqueued after the token (or on
+ * another stream) has already raised may be reported by this token rather
+ * than the next. Not allowed while `stream` is being captured
+ * (KVX_ERR_CAPTURE): read the status after replaying the graph. A token
+ * stays valid for the next 1,024 tokens of its device; after that,
+ * KVX_ERR_INVALID_ARG. */
 typedef struct kvx_status_token {
     uint64_t slot; /* opaque */
     uint64_t gen;  /* opaque */
@@ -440,7 +446,7 @@ kvx_status kvx_copy_batch_noalloc(const uint64_t *src_addrs, const uint64_t *dst
 
 /* Launch one CTA that waits on an mbarrier nothing ever completes, with the
  * same bounded wait the bulk kernel uses, limited to timeout_ns (1 ms..10 s).
- * The kernel gives up, sets the timeout bit of the status word and returns;
+ * The kernel gives up, sets the timeout flag of the device and returns;
  * a following kvx_stream_check returns KVX_ERR_TIMEOUT. Faults nothing. */
 kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
 

@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version_and_status_strings():
-    assert kvx.kvx_version() == kvx.KVX_VERSION == 3
+    assert kvx.kvx_version() == kvx.KVX_VERSION == 4
     names = [kvx.status_string(s) for s in range(10)]
     assert names[0] == "KVX_OK" and names[7] == "KVX_ERR_TIMEOUT" and names[9] == "KVX_ERR_CAPTURE"
     assert kvx.status_string(99) == "KVX_ERR_UNKNOWN"

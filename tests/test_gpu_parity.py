@@ -566,6 +566,21 @@ def test_status_tokens_pipelined():
         p.close()
 
 
+def test_status_token_refused_inside_capture():
+    # a status read waits on the host, so it cannot be part of a graph
+    gs = torch.cuda.Stream()
+    x = torch.zeros(16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        x.add_(1)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_status_enqueue(gs)
+    assert e.value.status == kvx.KVX_ERR_CAPTURE
+    graph.replay()
+    kvx.kvx_stream_check(None)
+    assert float(x[0]) == 1.0  # the capture itself went on
+
+
 def test_status_token_pending_then_timeout_then_expiry():
     s = torch.cuda.Stream()
     kvx.kvx_stream_check(s)
