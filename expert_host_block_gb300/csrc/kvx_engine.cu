@@ -18,6 +18,7 @@
 //   5. record the slot's event and return: enqueue-only (PegaFlow issue #408,
 //      follow-up §2).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -88,6 +89,7 @@ struct EnvSettings {
     int variant = KVX_VARIANT_AUTO;
     int cta_budget = 0;
     int log = 0;
+    bool nvtx = false;  // KVX_NVTX=1: NVTX ranges around each entry point and its packing
     std::vector<TableRow> table;  // KVX_TABLE rows, consulted before the built-in table
     std::string error;
 };
@@ -181,6 +183,12 @@ const EnvSettings &env()
             else
                 e.error = std::string("KVX_LOG=") + v + " is not 0, 1 or 2";
         }
+        if (const char *v = getenv("KVX_NVTX")) {
+            if (!strcmp(v, "0") || !strcmp(v, "1"))
+                e.nvtx = v[0] == '1';
+            else
+                e.error = std::string("KVX_NVTX=") + v + " is not 0 or 1";
+        }
         if (const char *v = getenv("KVX_PACK_THREADS")) {  // read by the worker pool
             char *end = nullptr;
             errno = 0;
@@ -199,6 +207,23 @@ const EnvSettings &env()
 }
 
 int log_level() { return env().log; }
+
+// An NVTX range for a profiler's timeline (KVX_NVTX=1), nothing otherwise.
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char *name) : on(env().nvtx)
+    {
+        if (on)
+            nvtxRangePushA(name);
+    }
+    ~NvtxRange()
+    {
+        if (on)
+            nvtxRangePop();
+    }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 std::atomic<int> g_validate_level{-1};
 
@@ -983,9 +1008,13 @@ kvx_status copy_batch_fast(const uint64_t *src, const uint64_t *dst, const uint6
     uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
     Launch l;
-    if (!pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk, &aligned16,
-                   &phases) ||
-        payload == 0 ||
+    bool packed;
+    {
+        NvtxRange pack_range("kvx pack");
+        packed = pack_fast(src, dst, sizes, n, s->host + kvx::kTableHeader, &chunks, &payload, &max_chunk,
+                           &aligned16, &phases);
+    }
+    if (!packed || payload == 0 ||
         resolve(dir, batch_shape(chunks, payload, aligned16, phases), want, &l) != KVX_OK) {
         ring_release(dev, s, stream, false);
         return KVX_OK;
@@ -1139,6 +1168,7 @@ kvx_status kvx_select_launch(const uint64_t *src, const uint64_t *dst, const uin
 kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n,
                              int dir, const kvx_launch *want, void *stream_)
 {
+    NvtxRange range("kvx_copy_batch");
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     kvx_status st = check_env();
     if (st != KVX_OK)
@@ -1173,7 +1203,10 @@ kvx_status kvx_copy_batch_ex(const uint64_t *src, const uint64_t *dst, const uin
     st = ring_acquire(dev, (size_t)chunks, &s);
     if (st != KVX_OK)
         return st;
-    pack(src, dst, sizes, n, s->host + kvx::kTableHeader, chunks);
+    {
+        NvtxRange pack_range("kvx pack");
+        pack(src, dst, sizes, n, s->host + kvx::kTableHeader, chunks);
+    }
     log_batch("kvx_copy_batch", dir, n, chunks, payload, l);
     return launch_from_slot(dev, s, dir, l, chunks, max_chunk, stream);
 }
@@ -1239,6 +1272,7 @@ kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
 kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const uint64_t *dst,
                                   const uint64_t *sizes, size_t n, int dir, void *stream_)
 {
+    NvtxRange range("kvx_upload_descriptors");
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!b)
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
@@ -1268,7 +1302,10 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
         KVX_CUDA_TRY(cudaEventSynchronize(b->upload_done));
         b->upload_recorded = false;
     }
-    pack(src, dst, sizes, n, b->host + kvx::kTableHeader, chunks);
+    {
+        NvtxRange pack_range("kvx pack");
+        pack(src, dst, sizes, n, b->host + kvx::kTableHeader, chunks);
+    }
     if (chunks)
         KVX_CUDA_TRY(cudaMemcpyAsync(b->dev, b->host, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
                                      cudaMemcpyHostToDevice, stream));
@@ -1285,6 +1322,7 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
 
 kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *stream_)
 {
+    NvtxRange range("kvx_copy_uploaded");
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!b)
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");

@@ -269,7 +269,8 @@ def test_validate_level_setting():
 
 @pytest.mark.parametrize("var,val", [("KVX_VARIANT", "tma"), ("KVX_VALIDATE", "yes"),
                                      ("KVX_CTA_BUDGET", "-4"), ("KVX_CTA_BUDGET", "12x"),
-                                     ("KVX_PACK_THREADS", "many"), ("KVX_PACK_THREADS", "99")])
+                                     ("KVX_PACK_THREADS", "many"), ("KVX_PACK_THREADS", "99"),
+                                     ("KVX_NVTX", "on"), ("KVX_NVTX", "2")])
 def test_unknown_env_values_are_errors(var, val):
     code = ("from expert_host_block_gb300 import kvx\n"
             "try:\n"
@@ -471,3 +472,14 @@ def test_select_launch_with_table_file_payload_rows(tmp_path):
     lines = out.stdout.strip().splitlines()
     assert "'cta_budget': 77, 'threads': 128, 'unroll': 4" in lines[0], out.stderr
     assert "'variant': 2, 'cta_budget': 456" in lines[1]  # 1 GiB: the file row does not apply
+
+
+def test_nvtx_switch_accepted():
+    # KVX_NVTX=1 only adds profiler ranges; host-only entry points behave the same
+    code = ("from expert_host_block_gb300 import kvx\n"
+            "print(kvx.kvx_select_launch([8], [16], [8], None, 'h2d')['variant'])\n"
+            "print(kvx.kvx_validate([8], [16], [12], None, 0, 0))\n")
+    for v in ("0", "1"):
+        out = _run_with_env(code, KVX_NVTX=v)
+        assert out.returncode == 0, out.stderr
+        assert out.stdout.split() == [str(kvx.KVX_VARIANT_LDG), str(kvx.KVX_ERR_ALIGN)]

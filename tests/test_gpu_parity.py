@@ -618,3 +618,16 @@ def test_d2d_table_row_follows_shape(n, odd, variant):
     finally:
         buf.close()
         p.close()
+
+
+def test_nvtx_ranges_on():
+    """KVX_NVTX=1 (NVTX ranges around the entry points, no tool attached): the copy is unchanged."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import __graft_entry__ as g\n"
+            "g.smoke()\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=root,
+                         env=dict(os.environ, KVX_NVTX="1"))
+    assert out.returncode == 0 and "smoke ok" in out.stdout, out.stdout + out.stderr
