@@ -427,15 +427,17 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
  *   - A batch that needs more than KVX_NOALLOC_MAX_CHUNKS chunks returns
  *     KVX_ERR_CAPACITY and enqueues nothing.
  *   - The first call on a device looks up the device address of the array
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress) with that device current and, unless another
+ *     kvx call did, registers the library's static page of error flags with
+ *     the driver (cudaHostRegister of existing memory, not an allocation);
+ *     make that first call before any stream capture on the device.
  *   - Every call shares the one array per device. Calls from several host
  *     threads are serialised until their copy is enqueued, so calls on one
  *     stream are safe; calls on different streams whose copies overlap on the
  *     GPU race on the array and may copy wrong bytes. Order them (one stream,
  *     or events) when they may overlap.
  *   - Nothing in the array has to start at zero: each call writes every record
- *     its kernel reads. */
+ *     its kernel reads, and the header record that holds the work counter. */
 #define KVX_NOALLOC_MAX_CHUNKS 65536u
 
 kvx_status kvx_copy_batch_noalloc(const uint64_t *src_addrs, const uint64_t *dst_addrs,
