@@ -1,7 +1,7 @@
 """Host threads calling the C ABI at once, each on its own stream, all bit-exact.
 
 ctypes releases the GIL during each call, so these threads really run
-kvx_copy_batch (staging ring, worker pool, status words) concurrently.
+kvx_copy_batch (staging ring, worker pool, status tokens and error flags) concurrently.
 """
 
 import threading
