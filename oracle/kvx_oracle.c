@@ -31,9 +31,10 @@
  *   - a zero-size descriptor copies nothing; n == 0 is the identity.
  *
  * Pins (tests/test_oracle.py): a pure-Python per-byte brute force over every
- * batch of up to two descriptors in 64-byte pools, sampled three-descriptor
+ * batch of up to two descriptors in 48-byte pools, sampled three-descriptor
  * batches, the canary / checksum / permutation invariants, published FNV-1a
- * test vectors, and planted mistakes that the pins must catch.
+ * test vectors, per-range checksums against FNV-1a of each slice, and
+ * planted mistakes that the pins must catch.
  */
 #include <stddef.h>
 #include <stdint.h>

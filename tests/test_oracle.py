@@ -207,3 +207,62 @@ def test_pins_catch_planted_mistakes(tiny_pools, mutant):
             caught = True
             break
     assert caught, mutant.__name__
+
+
+# ---- range_checksums: each entry is FNV-1a of exactly its own slice --------
+#
+# fnv1a64 is pinned by the published vectors above; these tests pin the
+# per-range wrapper to it (one slice per entry, each slice's own offset and
+# size), so a wrapper that drops or reuses a size, or an offset, fails.
+
+def _checksum_ranges(g, pool_bytes, n):
+    off = (8 * g.integers(0, pool_bytes // 8, n)).astype(np.uint64)
+    room = pool_bytes - off
+    sz = np.minimum((8 * g.integers(0, 96, n)).astype(np.uint64), room)
+    sz[::5] = 0  # zero-size ranges among the others
+    return off, sz
+
+
+def test_range_checksums_each_entry_is_its_slice():
+    g = np.random.default_rng(11)
+    pool = g.integers(0, 256, 1 << 16, dtype=np.uint8)
+    off, sz = _checksum_ranges(g, pool.size, 300)
+    assert len(set(int(z) for z in sz)) > 20  # many different lengths in one call
+    got = oracle.range_checksums(pool, off, sz)
+    for i, (o, z) in enumerate(zip(off, sz)):
+        assert int(got[i]) == oracle.fnv1a64(pool[int(o):int(o + z)]), i
+
+
+def test_range_checksums_golden_foobar_and_empty(golden):
+    vec = golden("fnv1a64_vectors.txt")
+    pool = np.full(64, 0x5A, dtype=np.uint8)
+    pool[16:22] = np.frombuffer(b"foobar", dtype=np.uint8)
+    pool[40] = ord("a")
+    got = oracle.range_checksums(pool, [16, 40, 0, 30], [6, 1, 0, 0])
+    assert int(got[0]) == int(vec['"foobar"'][0], 16)
+    assert int(got[1]) == int(vec['"a"'][0], 16)
+    assert int(got[2]) == int(vec['""'][0], 16)  # an empty range hashes to the offset basis
+    assert int(got[3]) == int(vec['""'][0], 16)
+
+
+def _mutant_checksums_ignore_sizes(pool, off, sz):
+    return oracle.range_checksums(pool, off, np.zeros_like(sz))
+
+
+def _mutant_checksums_first_size(pool, off, sz):
+    return oracle.range_checksums(pool, off, np.minimum(np.full_like(sz, sz[0]), pool.size - off))
+
+
+def _mutant_checksums_first_offset(pool, off, sz):
+    return oracle.range_checksums(pool, np.full_like(off, off[0]), np.minimum(sz, pool.size - off[0]))
+
+
+@pytest.mark.parametrize("mutant", [_mutant_checksums_ignore_sizes, _mutant_checksums_first_size,
+                                    _mutant_checksums_first_offset])
+def test_range_checksum_pins_catch_planted_mistakes(mutant):
+    g = np.random.default_rng(12)
+    pool = g.integers(0, 256, 1 << 12, dtype=np.uint8)
+    off, sz = _checksum_ranges(g, pool.size, 40)
+    bad = mutant(pool, off, sz)
+    want = [oracle.fnv1a64(pool[int(o):int(o + z)]) for o, z in zip(off, sz)]
+    assert [int(x) for x in bad] != want, mutant.__name__
