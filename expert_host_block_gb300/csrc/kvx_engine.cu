@@ -1785,6 +1785,15 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
         return st;
     if (chunks == 0)
         return KVX_OK;
+    // Under capture the table upload would become a graph node that reads the
+    // shared host array at replay time, by then holding another call's records.
+    bool cap = false;
+    st = is_capturing(stream, &cap);
+    if (st != KVX_OK)
+        return st;
+    if (cap)
+        return fail(KVX_ERR_CAPTURE,
+                    "kvx_copy_batch_noalloc uploads from a shared host array; capture kvx_copy_uploaded instead");
     int dev = 0;
     KVX_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices)

@@ -135,7 +135,11 @@ typedef struct kvx_desc_buf kvx_desc_buf;
 /* ---- the batch copy ----------------------------------------------------- */
 
 /* Copy a batch: validate, chunk, pack, upload the chunk table and launch the
- * copy kernel on `stream`. `dir` is a kvx_dir; it selects the table row and
+ * copy kernel on `stream`: one descriptor upload and one copy-kernel launch in
+ * place of one memcpy per fragment (PegaFlow issue #408, §Summary), with the
+ * three address/size arrays of the vLLM wrapper `swap_blocks_batch` (vLLM PR
+ * #42212 report, §实现拆解 item 1). Enqueue-only (PegaFlow issue #408,
+ * follow-up §2). `dir` is a kvx_dir; it selects the table row and
  * what validation level 2 checks (data moves through unified addresses in
  * every direction). `cta_budget`: 0 = calibrated default, > 0 = at most that
  * many CTAs, < 0 = KVX_ERR_INVALID_ARG. Not allowed during stream capture
@@ -154,19 +158,33 @@ kvx_status kvx_copy_batch(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                           const uint64_t *sizes, size_t n, int dir, int cta_budget,
                           void *stream);
 
-/* kvx_copy_batch with an explicit launch configuration (NULL = all table). */
+/* kvx_copy_batch with an explicit launch configuration (NULL = all table):
+ * the per-device grid limit the pages ask to expose instead of a constant
+ * (PegaFlow issue #408, follow-up §Proposed direction, `KernelOptions`
+ * `max_grid_blocks`). */
 kvx_status kvx_copy_batch_ex(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                              const uint64_t *sizes, size_t n, int dir,
                              const kvx_launch *launch, void *stream);
 
 /* ---- reusable descriptor buffers (pinned staging + device table) -------- */
+/* The vLLM transfer keeps three pinned descriptor buffers that it allocates
+ * once and reuses for every transfer, so that the H2D copy of the descriptors
+ * is truly asynchronous and no transfer allocates (vLLM PR #42212 report,
+ * §实现拆解 item 3, `_new_descriptor_buffers`; §评论区精华, pinned memory).
+ * A kvx_desc_buf is that buffer, holding the packed chunk table instead of
+ * the three arrays, plus its device copy, so that a copy over it is a
+ * fixed-shape launch with no host work (FreeToken issue #751, §What we
+ * changed: fixed-shape, CUDA-graph capturable). */
 
 /* Create a buffer for up to max_chunks chunk records (1..KVX_MAX_CHUNKS) on
- * the current device. Allocates device and pinned host memory (synchronous). */
+ * the current device. Allocates device and pinned host memory (synchronous),
+ * once, for reuse by every upload (vLLM PR #42212 report, §实现拆解 item 3). */
 kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out);
 
 /* Validate, chunk and pack a batch into the buffer's pinned staging area and
- * enqueue its upload on `stream`. Waits on the host only while the buffer's
+ * enqueue its upload on `stream`: the one descriptor upload of a batch
+ * (PegaFlow issue #408, §Summary), into the reused pinned buffer (vLLM PR
+ * #42212 report, §实现拆解 item 3). Waits on the host only while the buffer's
  * previous upload is still in flight. The caller orders this upload after any
  * kvx_copy_uploaded of the same buffer that is still running on another
  * stream (same stream: ordered already). Not allowed during capture. */
@@ -175,7 +193,9 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
                                   size_t n, int dir, void *stream);
 
 /* Launch the copy kernel over the uploaded table. No host work besides the
- * launch: fixed shape, allowed inside CUDA graph capture. `cta_budget` as in
+ * launch: fixed shape, allowed inside CUDA graph capture (FreeToken issue
+ * #751, §What we changed: the launch is fixed-shape and CUDA-graph
+ * capturable). `cta_budget` as in
  * kvx_copy_batch. Two copies of one buffer must not run at the same time (a
  * dynamic-assignment copy keeps its work counter in the buffer): outside
  * capture, each copy first makes `stream` wait for the buffer's previous copy
@@ -183,15 +203,21 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
  * order. */
 kvx_status kvx_copy_uploaded(kvx_desc_buf *buf, int cta_budget, void *stream);
 
-/* kvx_copy_uploaded with an explicit launch configuration (NULL = table). */
+/* kvx_copy_uploaded with an explicit launch configuration (NULL = table): the
+ * bounded, device-specific grid of PegaFlow issue #408, follow-up §Proposed
+ * direction (`KernelOptions`). */
 kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *buf, const kvx_launch *launch, void *stream);
 
 /* Chunks and payload bytes of the last upload, and the launch configuration
- * the table selected for it. Any output pointer may be NULL. */
+ * the table selected for it (the device-aware profile's choice: PegaFlow
+ * issue #408, follow-up §Proposed direction). Any output pointer may be
+ * NULL. */
 kvx_status kvx_desc_buf_info(const kvx_desc_buf *buf, size_t *n_chunks,
                              uint64_t *payload_bytes, kvx_launch *selected);
 
-/* Wait for the buffer's last upload and last copy, then free it. */
+/* Wait for the buffer's last upload and last copy, then free it. The buffers
+ * live as long as their owner wants them reused (vLLM PR #42212 report,
+ * §实现拆解 item 3: allocated once and reused, not per transfer). */
 kvx_status kvx_desc_buf_destroy(kvx_desc_buf *buf);
 
 /* ---- descriptor lists that live on the device ---------------------------- */
@@ -329,6 +355,10 @@ kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *ou
 kvx_status kvx_set_validate_level(int level);
 int kvx_get_validate_level(void);
 
+/* The name of a kvx_status ("KVX_ERR_TIMEOUT"...), for the completion status
+ * that the enqueue-only contract reads after the fact (PegaFlow issue #408,
+ * follow-up §2: record completion, query it later). Never NULL:
+ * "KVX_ERR_UNKNOWN" for a value that is not a kvx_status. */
 const char *kvx_status_string(int status);
 /* Message of the last non-OK status returned in the calling thread. */
 const char *kvx_last_error(void);
@@ -336,8 +366,11 @@ int kvx_version(void); /* KVX_VERSION_MAJOR * 100 + KVX_VERSION_MINOR */
 
 /* ---- device status, memory ---------------------------------------------- */
 
-/* Synchronise `stream`, then read and clear the device's error flags, which
- * kernels set (a bounded wait that gave up, an inconsistent chunk record, a
+/* Synchronise `stream`, then read and clear the device's error flags: the
+ * completion read that the enqueue-only copy leaves to the caller (PegaFlow
+ * issue #408, follow-up §2: the transfer backend contract is enqueue-only,
+ * so completion is recorded and read later, outside submit). Kernels set the
+ * flags (a bounded wait that gave up, an inconsistent chunk record, a
  * device-list count above capacity or a bad device-list descriptor). The
  * flags live in a page of mapped pinned host memory that kvx registers with
  * the driver on its first use in the process (a static page, no allocation);
@@ -417,8 +450,11 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
  * allocation or a device-wide synchronisation in the middle of a step.
  *
  * kvx_copy_batch_noalloc takes the same arguments and moves the same bytes as
- * kvx_copy_batch, with the same validation and error rules, but calls no
- * cudaMalloc, cudaFree, cudaHostAlloc or other allocating routine. Its chunk
+ * kvx_copy_batch, with the same validation and error rules, but makes no CUDA
+ * device or pinned-host allocation: no cudaMalloc, cudaFree, cudaHostAlloc or
+ * cudaHostRegister of new memory. (Host heap use is not excluded: validation
+ * levels 1 and 2 sort a heap copy of the ranges, and the first pack of 32 Ki
+ * records or more may start the library's packing threads.) Its chunk
  * table lives in a fixed array of KVX_NOALLOC_MAX_CHUNKS records (2 MiB) in the
  * library's own device memory, which every GPU that loads the library holds
  * until the process exits; the records are packed into a fixed host array of
@@ -426,11 +462,14 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
  * array, which the runtime stages before returning.
  *   - A batch that needs more than KVX_NOALLOC_MAX_CHUNKS chunks returns
  *     KVX_ERR_CAPACITY and enqueues nothing.
+ *   - Not allowed while `stream` is being captured (KVX_ERR_CAPTURE): the
+ *     table upload reads the shared host array, which a replayed graph would
+ *     read again with whatever another call had packed there since. Capture
+ *     kvx_copy_uploaded over a kvx_desc_buf instead.
  *   - The first call on a device looks up the device address of the array
  *     (cudaGetSymbolAddress) with that device current and, unless another
  *     kvx call did, registers the library's static page of error flags with
- *     the driver (cudaHostRegister of existing memory, not an allocation);
- *     make that first call before any stream capture on the device.
+ *     the driver (cudaHostRegister of existing memory, not an allocation).
  *   - Every call shares the one array per device. Calls from several host
  *     threads are serialised until their copy is enqueued, so calls on one
  *     stream are safe; calls on different streams whose copies overlap on the

@@ -40,6 +40,36 @@ def test_header_declares_what_binding_lists():
     assert _declared() == sorted(kvx.EXPORTS)
 
 
+# The boundary calls (the batch copy, the reusable descriptor buffers, the
+# completion read, the direct baseline) and the comment block written right
+# above each declaration.
+BOUNDARY_CALLS = ("kvx_copy_batch", "kvx_copy_batch_ex", "kvx_desc_buf_create", "kvx_upload_descriptors",
+                  "kvx_copy_uploaded", "kvx_copy_uploaded_ex", "kvx_desc_buf_info", "kvx_desc_buf_destroy",
+                  "kvx_stream_check", "kvx_status_string", "kvx_copy_batch_memcpy", "kvx_copy_contiguous")
+PAGE = re.compile(r"(PegaFlow issue #408|vLLM PR #42212 report|FreeToken issue #751)[^§]{0,80}§")
+
+
+def _comment_above(text, name):
+    m = re.search(r"\b" + name + r"\s*\(", re.sub(r"/\*.*?\*/", lambda c: " " * len(c.group()), text, flags=re.S))
+    assert m, name
+    end = text.rfind("*/", 0, m.start())
+    start = text.rfind("/*", 0, end)
+    between = text[end + 2:m.start()]
+    assert "/*" not in between and ";" not in between, f"{name}: no comment block right above it"
+    return text[start:end + 2]
+
+
+def test_boundary_declarations_cite_a_page_and_section():
+    text = open(os.path.join(ROOT, "include", "kvx.h")).read()
+    for name in BOUNDARY_CALLS:
+        block = " ".join(re.sub(r"^\s*\*(?!/)", " ", _comment_above(text, name), flags=re.M).split())
+        assert PAGE.search(block), f"{name}: its comment names no page and section"
+    # the one entry point with no counterpart on the pages says so instead
+    noalloc = text[text.index("a batch copy that allocates nothing"):text.index("kvx_copy_batch_noalloc(")]
+    noalloc = " ".join(re.sub(r"^\s*\*(?!/)", " ", noalloc, flags=re.M).split())
+    assert "The pages have no counterpart" in noalloc
+
+
 def test_library_exports_every_declared_symbol():
     lib = kvx.lib()
     for name in _declared():

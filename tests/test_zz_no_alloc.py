@@ -14,7 +14,7 @@ holding the first call's tail) go once through kvx_copy_batch into one
 destination pool and once through kvx_copy_batch_noalloc into an identical
 pool; the two pools must match byte for byte (the bit-exact tolerance of every
 copy test here), and both must match the oracle. A batch one chunk too large
-is refused before anything is enqueued.
+is refused before anything is enqueued, and so is a call during stream capture.
 
 This file sorts last so that a run stopping at its first failure has run every
 other test first; it also passes alone in a fresh process.
@@ -89,5 +89,32 @@ def test_noalloc_refuses_more_than_its_table():
         assert e.value.status == kvx.KVX_ERR_CAPACITY
         torch.cuda.synchronize()
         assert np.array_equal(p.snapshot("dst"), before)
+    finally:
+        p.close()
+
+
+def test_noalloc_refused_inside_capture():
+    # The upload reads the one shared host array: a captured upload would read
+    # it again at replay time, after other calls had packed other records there.
+    p = Pools({"src": W.PoolSpec("src", "device", 4 * W.MIB, "random", (79,)),
+               "dst": W.PoolSpec("dst", "device", 4 * W.MIB, "canary")})
+    try:
+        before = p.snapshot("dst")
+        s = np.uint64(p.base("src")) + np.arange(64, dtype=np.uint64) * np.uint64(4096)
+        d = np.uint64(p.base("dst")) + np.arange(64, dtype=np.uint64) * np.uint64(4096)
+        z = np.full(64, 4096, dtype=np.uint64)
+        gs = torch.cuda.Stream()
+        x = torch.zeros(16, device="cuda")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            x.add_(1)
+            with pytest.raises(kvx.KvxError) as e:
+                kvx.kvx_copy_batch_noalloc(s, d, z, None, "d2d", 0, gs)
+        assert e.value.status == kvx.KVX_ERR_CAPTURE
+        graph.replay()
+        torch.cuda.synchronize()
+        kvx.kvx_stream_check(None)
+        assert float(x[0]) == 1.0                 # the capture itself went on
+        assert np.array_equal(p.snapshot("dst"), before)   # and enqueued no copy
     finally:
         p.close()
