@@ -90,6 +90,7 @@ struct EnvSettings {
     int cta_budget = 0;
     int log = 0;
     bool nvtx = false;  // KVX_NVTX=1: NVTX ranges around each entry point and its packing
+    bool pdl = true;    // KVX_PDL=0: launch the copy kernels without programmatic dependent launch
     std::vector<TableRow> table;  // KVX_TABLE rows, consulted before the built-in table
     std::string error;
 };
@@ -188,6 +189,12 @@ const EnvSettings &env()
                 e.nvtx = v[0] == '1';
             else
                 e.error = std::string("KVX_NVTX=") + v + " is not 0 or 1";
+        }
+        if (const char *v = getenv("KVX_PDL")) {
+            if (!strcmp(v, "0") || !strcmp(v, "1"))
+                e.pdl = v[0] == '1';
+            else
+                e.error = std::string("KVX_PDL=") + v + " is not 0 or 1";
         }
         if (const char *v = getenv("KVX_PACK_THREADS")) {  // read by the worker pool
             char *end = nullptr;
@@ -646,6 +653,7 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     out->store_policy = policy;
     out->assign = assign;
     out->matched = shape.matched;
+    out->pdl = e.pdl;
     return KVX_OK;
 }
 

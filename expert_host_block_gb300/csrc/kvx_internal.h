@@ -43,6 +43,7 @@ struct Launch {
     int store_policy;  // LDG store cache policy
     int assign;        // LDG: KVX_ASSIGN_STATIC or KVX_ASSIGN_DYNAMIC
     bool matched;      // LDG: every chunk's src and dst agree mod 16 (decided from the packed batch)
+    bool pdl;          // launch with programmatic stream serialisation (KVX_PDL, default on)
 };
 
 // Every device chunk table starts with one header record that holds the

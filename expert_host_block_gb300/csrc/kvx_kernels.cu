@@ -31,8 +31,21 @@
 // have the same phase mod 16, a chunk is an 8-byte head, a 16-byte-word body
 // and an 8-byte tail; otherwise aligned 16-byte source words are re-paired
 // across neighbouring lanes into aligned 16-byte destination words.
+//
+// Back to back on a stream (programmatic dependent launch): every copy kernel
+// is launched with programmatic stream serialisation and lets the grid after
+// it launch as soon as all of its own CTAs are running, so the launch of the
+// next batch overlaps this one instead of following its completion. A copy
+// kernel reads only its chunk table before it waits for the grid before it
+// (griddepcontrol.wait: that grid has completed and its writes are visible);
+// a table is written by the host or by a copy on the stream, never by a
+// kernel, so the only thing read early is already final. Payload, the
+// dynamic-assignment counter and device-list plans are touched only after the
+// wait. A grid launched without the attribute returns from the wait at once.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "kvx_internal.h"
 
@@ -50,6 +63,22 @@ __device__ __forceinline__ void report(unsigned *err, unsigned kind)
 }
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Allow the grid launched after this one on the stream to start (it then runs
+// only up to its own pdl_wait until this grid completes).
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible to this grid.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // ---- global memory access (inline PTX) ----------------------------------
 
@@ -315,12 +344,14 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
                                                             uint32_t n_chunks, uint32_t passes,
                                                             unsigned long long *ctr, unsigned *err)
 {
+    pdl_trigger();
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t wpb = blockDim.x >> 5;
     const uint64_t gwarp = (uint64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const uint64_t nwarps = (uint64_t)gridDim.x * wpb;
     const uint64_t n_units = (uint64_t)n_chunks * passes;
     if (ctr == nullptr) {
+        bool waited = false;  // the first 32 records load before the wait
         for (uint64_t base = gwarp; base < n_units; base += 32u * nwarps) {
             const uint64_t mine = base + (uint64_t)lane * nwarps;
             Rec r = {0, 0, 0};
@@ -328,6 +359,10 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
             if (mine < n_units)
                 r = unit_rec(tab, mine, n_chunks, PassBytes<U>::value, &k, err);
             const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
+            if (!waited) {
+                pdl_wait();
+                waited = true;
+            }
             for (int j = 0; j < cnt; ++j) {
                 const Rec c = shfl_rec(r, j);
                 const uint32_t kk = __shfl_sync(kFull, k, j);
@@ -342,11 +377,12 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
     unsigned long long nx = 0;
     Rec rc = {0, 0, 0};
     uint32_t kc = 0;
-    if (lane == 0) {
+    if (lane == 0 && cur < n_units)
+        rc = unit_rec(tab, cur, n_chunks, PassBytes<U>::value, &kc, err);
+    // the previous copy over this table zeroes the counter as it ends
+    pdl_wait();
+    if (lane == 0)
         nx = nwarps + atomicAdd(&ctr[0], 1ull);
-        if (cur < n_units)
-            rc = unit_rec(tab, cur, n_chunks, PassBytes<U>::value, &kc, err);
-    }
     while (cur < n_units) {
         unsigned long long nn = 0;
         Rec rn = {0, 0, 0};
@@ -517,6 +553,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t D = S / 2;  // loads ahead, >= 1 because S >= 2
 
+    pdl_trigger();
     if (lane == 0) {
         for (uint32_t s = 0; s < S; ++s)
             mbar_init(bar0 + 8u * s, 1);
@@ -541,6 +578,7 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     uint32_t mask_a = load_batch(0);   // chunks [a0, a0 + 32)
     uint32_t mask_b = load_batch(32);  // chunks [a0 + 32, a0 + 64); the look-ahead k + D < a0 + 64
     __syncwarp();
+    pdl_wait();  // records only before this point
     auto eligible = [&](uint64_t c) {
         const uint64_t o = c - a0;
         return ((o < 32u ? mask_a >> o : mask_b >> (o - 32u)) & 1u) != 0;
@@ -638,6 +676,10 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
     __shared__ uint64_t warp_sums[32];
     __shared__ uint64_t s_carry;
     __shared__ uint32_t s_max, s_bad;
+    // the list may come from the kernel before this one, and the copy before
+    // may still read this list's plan
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tid = threadIdx.x, lane = tid & 31u, wid = tid >> 5;
     const uint32_t nwarps = blockDim.x >> 5;
     uint32_t n = *count;
@@ -754,6 +796,8 @@ __global__ void __launch_bounds__(512) kvx_copy_devlist_kernel(
     const uint64_t *__restrict__ offsets, bool dynamic)
 {
     __shared__ uint64_t s_off[kSmemOffsets];
+    pdl_trigger();
+    pdl_wait();  // the plan kernel's results
     const uint64_t total = meta->total;
     const uint32_t n = meta->n;
     if (total == 0)
@@ -835,29 +879,45 @@ __global__ void kvx_wait_selftest_kernel(uint64_t timeout_ns, unsigned *err)
     __syncwarp();
 }
 
+// Launch a kernel on `s`, with programmatic stream serialisation when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), int ctas, int threads, size_t smem, cudaStream_t s,
+                     Args &&...args)
+{
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int U, int P>
-cudaError_t launch_ldg(int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
+cudaError_t launch_ldg(bool pdl, int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
                        unsigned long long *ctr, bool matched, unsigned *err, cudaStream_t s)
 {
     if (matched)
-        kvx_copy_ldg_kernel<U, P, true><<<ctas, threads, 0, s>>>(t, n, passes, ctr, err);
-    else
-        kvx_copy_ldg_kernel<U, P, false><<<ctas, threads, 0, s>>>(t, n, passes, ctr, err);
-    return cudaGetLastError();
+        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, true>, ctas, threads, 0, s, t, n, passes, ctr, err);
+    return launch_k(pdl, kvx_copy_ldg_kernel<U, P, false>, ctas, threads, 0, s, t, n, passes, ctr, err);
 }
 
 template <int U>
-cudaError_t launch_ldg_p(int p, int ctas, int threads, const kvx_chunk *t, uint32_t n,
-                         uint32_t passes, unsigned long long *ctr, bool matched, unsigned *err, cudaStream_t s)
+cudaError_t launch_ldg_p(const Launch &l, int ctas, const kvx_chunk *t, uint32_t n,
+                         uint32_t passes, unsigned long long *ctr, unsigned *err, cudaStream_t s)
 {
-    switch (p) {
-    case 1: return launch_ldg<U, 1>(ctas, threads, t, n, passes, ctr, matched, err, s);
-    case 2: return launch_ldg<U, 2>(ctas, threads, t, n, passes, ctr, matched, err, s);
-    default: return launch_ldg<U, 0>(ctas, threads, t, n, passes, ctr, matched, err, s);
+    switch (l.store_policy) {
+    case 1: return launch_ldg<U, 1>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
+    case 2: return launch_ldg<U, 2>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
+    default: return launch_ldg<U, 0>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
     }
 }
 
-cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n, uint32_t max_chunk_len,
+cudaError_t launch_bulk(bool pdl, int ctas, int ring_units, const kvx_chunk *t, uint32_t n, uint32_t max_chunk_len,
                         unsigned *err, cudaStream_t s)
 {
     const uint32_t ring = (uint32_t)bulk_smem_bytes(ring_units);
@@ -871,21 +931,19 @@ cudaError_t launch_bulk(int ctas, int ring_units, const kvx_chunk *t, uint32_t n
                                          (int)ring);
     if (e != cudaSuccess)
         return e;
-    kvx_copy_bulk_kernel<<<ctas, 32, ring, s>>>(t, n, stage, S, kBulkWaitNs, err);
-    return cudaGetLastError();
+    return launch_k(pdl, kvx_copy_bulk_kernel, ctas, 32, ring, s, t, n, stage, S, kBulkWaitNs, err);
 }
 
 template <int U>
-cudaError_t launch_devlist_p(int p, int ctas, int threads, const uint64_t *src, const uint64_t *dst,
+cudaError_t launch_devlist_p(const Launch &l, const uint64_t *src, const uint64_t *dst,
                             const uint64_t *sizes, DevListMeta *meta, const uint64_t *offsets, bool dyn,
                             cudaStream_t s)
 {
-    switch (p) {
-    case 1: kvx_copy_devlist_kernel<U, 1><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
-    case 2: kvx_copy_devlist_kernel<U, 2><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
-    default: kvx_copy_devlist_kernel<U, 0><<<ctas, threads, 0, s>>>(src, dst, sizes, meta, offsets, dyn); break;
+    switch (l.store_policy) {
+    case 1: return launch_k(l.pdl, kvx_copy_devlist_kernel<U, 1>, l.ctas, l.threads, 0, s, src, dst, sizes, meta, offsets, dyn);
+    case 2: return launch_k(l.pdl, kvx_copy_devlist_kernel<U, 2>, l.ctas, l.threads, 0, s, src, dst, sizes, meta, offsets, dyn);
+    default: return launch_k(l.pdl, kvx_copy_devlist_kernel<U, 0>, l.ctas, l.threads, 0, s, src, dst, sizes, meta, offsets, dyn);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -932,15 +990,15 @@ cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
     const int ctas = work_ctas(l, n_chunks, max_chunk_len);
     const kvx_chunk *recs = table + kTableHeader;
     if (l.variant == KVX_VARIANT_BULK) {
-        return launch_bulk(ctas, l.stages, recs, n_chunks, max_chunk_len, err, stream);
+        return launch_bulk(l.pdl, ctas, l.stages, recs, n_chunks, max_chunk_len, err, stream);
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
     unsigned long long *ctr =
         ldg_dynamic(l, n_chunks, max_chunk_len) ? reinterpret_cast<unsigned long long *>(table) : nullptr;
     switch (l.unroll) {
-    case 2: return launch_ldg_p<2>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
-    case 4: return launch_ldg_p<4>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
-    default: return launch_ldg_p<8>(l.store_policy, ctas, l.threads, recs, n_chunks, passes, ctr, l.matched, err, stream);
+    case 2: return launch_ldg_p<2>(l, ctas, recs, n_chunks, passes, ctr, err, stream);
+    case 4: return launch_ldg_p<4>(l, ctas, recs, n_chunks, passes, ctr, err, stream);
+    default: return launch_ldg_p<8>(l, ctas, recs, n_chunks, passes, ctr, err, stream);
     }
 }
 
@@ -948,15 +1006,15 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
                            const uint64_t *sizes, const uint32_t *count, uint32_t max_n,
                            DevListMeta *meta, uint64_t *offsets, unsigned *err, cudaStream_t stream)
 {
-    kvx_devlist_plan_kernel<<<1, 1024, 0, stream>>>(src, dst, sizes, count, max_n, meta, offsets, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_k(l.pdl, kvx_devlist_plan_kernel, 1, 1024, 0, stream, src, dst, sizes, count, max_n,
+                             meta, offsets, err);
     if (e != cudaSuccess)
         return e;
     const bool dyn = l.assign == KVX_ASSIGN_DYNAMIC;
     switch (l.unroll) {
-    case 2: return launch_devlist_p<2>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
-    case 4: return launch_devlist_p<4>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
-    default: return launch_devlist_p<8>(l.store_policy, l.ctas, l.threads, src, dst, sizes, meta, offsets, dyn, stream);
+    case 2: return launch_devlist_p<2>(l, src, dst, sizes, meta, offsets, dyn, stream);
+    case 4: return launch_devlist_p<4>(l, src, dst, sizes, meta, offsets, dyn, stream);
+    default: return launch_devlist_p<8>(l, src, dst, sizes, meta, offsets, dyn, stream);
     }
 }
 

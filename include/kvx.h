@@ -43,6 +43,18 @@
  *     returns. The payload must stay valid until the stream reaches the copy.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream) of the
  *     device that is current in the calling thread.
+ *   - Back-to-back copies: every copy kernel is launched with programmatic
+ *     stream serialisation (programmatic dependent launch). A copy may start
+ *     launching while the kernel before it on `stream` still runs; until that
+ *     kernel has completed and its writes are visible it reads only its own
+ *     chunk table, never payload. The copy also lets the next kernel on
+ *     `stream` launch early: a kernel launched after a kvx copy with
+ *     cudaLaunchAttributeProgrammaticStreamSerialization must call
+ *     cudaGridDependencySynchronize() before it reads the copy's destination
+ *     or writes its source, as that attribute requires of every kernel.
+ *     Kernels launched without the attribute, copy-engine work and events
+ *     are ordered as usual. The environment variable KVX_PDL=0 launches the
+ *     copy kernels without the attribute.
  *   - Errors: a non-KVX_OK status means nothing was enqueued, except
  *     KVX_ERR_CUDA from a launch, which may follow a completed table upload.
  *     kvx_last_error() gives a one-line message for the calling thread.

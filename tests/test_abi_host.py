@@ -300,7 +300,8 @@ def test_validate_level_setting():
 @pytest.mark.parametrize("var,val", [("KVX_VARIANT", "tma"), ("KVX_VALIDATE", "yes"),
                                      ("KVX_CTA_BUDGET", "-4"), ("KVX_CTA_BUDGET", "12x"),
                                      ("KVX_PACK_THREADS", "many"), ("KVX_PACK_THREADS", "99"),
-                                     ("KVX_NVTX", "on"), ("KVX_NVTX", "2")])
+                                     ("KVX_NVTX", "on"), ("KVX_NVTX", "2"), ("KVX_PDL", "yes"),
+                                     ("KVX_PDL", "2")])
 def test_unknown_env_values_are_errors(var, val):
     code = ("from expert_host_block_gb300 import kvx\n"
             "try:\n"
