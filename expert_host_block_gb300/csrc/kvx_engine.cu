@@ -1052,6 +1052,7 @@ struct kvx_desc_buf {
     cudaEvent_t last_use = nullptr;
     bool upload_recorded = false;
     bool use_recorded = false;
+    unsigned long long last_stream = 0;  // cudaStreamGetId of the stream of the last copy
     uint32_t n_chunks = 0;
     uint32_t max_chunk = 0;
     uint64_t payload = 0;
@@ -1368,18 +1369,25 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
-    // two copies over one table must not overlap: order this one after the
-    // buffer's previous copy (a no-op when that ran earlier on this stream;
-    // stream handles are not compared, since a destroyed stream's handle can
-    // come back for a new one)
-    if (!cap && b->use_recorded)
-        KVX_CUDA_TRY(cudaStreamWaitEvent(stream, b->last_use, 0));
+    // Two copies over one table must not overlap: order this one after the
+    // buffer's previous copy. On the same stream they are ordered already, and
+    // waiting on that copy's event as well would make this launch wait for its
+    // completion instead of overlapping its tail (programmatic dependent
+    // launch). Streams are compared by cudaStreamGetId, which is never reused,
+    // not by handle: a destroyed stream's handle can come back for a new one.
+    unsigned long long sid = 0;
+    if (!cap) {
+        KVX_CUDA_TRY(cudaStreamGetId(stream, &sid));
+        if (b->use_recorded && b->last_stream != sid)
+            KVX_CUDA_TRY(cudaStreamWaitEvent(stream, b->last_use, 0));
+    }
     cudaError_t e = kvx::launch_copy(l, b->dev, b->n_chunks, b->max_chunk, b->err, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "copy kernel launch");
     if (!cap) {
         KVX_CUDA_TRY(cudaEventRecord(b->last_use, stream));
         b->use_recorded = true;
+        b->last_stream = sid;
     }
     return KVX_OK;
 }
