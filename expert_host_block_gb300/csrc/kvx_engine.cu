@@ -615,6 +615,14 @@ BatchShape batch_shape(uint64_t chunks, uint64_t payload, uint64_t aligned16, ui
     return b;
 }
 
+// Whether an LDG copy of this direction and payload prefetches its sources into
+// L2 while it waits for the grid before it: D2D (sources in HBM) of at most
+// kvx::kPrefetchMaxPayload bytes (an unknown payload is ~0: no).
+bool prefetch_for(int dir, uint64_t payload)
+{
+    return env().pdl && dir == KVX_D2D && payload <= kvx::kPrefetchMaxPayload;
+}
+
 // Merge explicit settings over env over table and check them.
 kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Launch *out)
 {
@@ -654,6 +662,7 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     out->assign = assign;
     out->matched = shape.matched;
     out->pdl = e.pdl;
+    out->prefetch = prefetch_for(dir, shape.payload);
     return KVX_OK;
 }
 
@@ -1363,6 +1372,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     if (st != KVX_OK)
         return st;
     l.matched = b->matched;
+    l.prefetch = prefetch_for(b->dir, b->payload);
     if (b->n_chunks == 0)
         return KVX_OK;
     bool cap = false;

@@ -80,6 +80,16 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Ask for [p, p + bytes) to be brought into L2 (p and bytes multiples of 16).
+// A hint: it returns no data and needs no completion. Issued before pdl_wait it
+// reads nothing stale, because the L2 is where every write to device memory
+// lands: a write of the grid before this one updates the line after the
+// prefetch brought it in.
+__device__ __forceinline__ void prefetch_l2(uint64_t p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- global memory access (inline PTX) ----------------------------------
 
 __device__ __forceinline__ uint4 ld16(const unsigned char *p)
@@ -339,10 +349,16 @@ __device__ __forceinline__ Rec unit_rec(const kvx_chunk *__restrict__ tab, uint6
     return r;
 }
 
+// Static assignment with kLdgPrefetch (D2D batches small enough for their
+// sources to sit in L2 beside the previous batch's writes): before the wait,
+// every lane asks L2 for the source bytes of the unit whose record it holds,
+// so a batch launched early fetches its first data while the one before it
+// drains (4,096 x 8 KiB back to back: 0.83 -> 0.90 of HBM).
 template <int U, int P, bool M>
 __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
                                                             uint32_t n_chunks, uint32_t passes,
-                                                            unsigned long long *ctr, unsigned *err)
+                                                            unsigned long long *ctr, unsigned *err,
+                                                            uint32_t flags)
 {
     pdl_trigger();
     const uint32_t lane = threadIdx.x & 31u;
@@ -360,6 +376,14 @@ __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__re
                 r = unit_rec(tab, mine, n_chunks, PassBytes<U>::value, &k, err);
             const int cnt = __popc(__ballot_sync(kFull, mine < n_units));
             if (!waited) {
+                if ((flags & kLdgPrefetch) && r.l) {
+                    // the 16-byte blocks holding this unit's pass (no byte outside them)
+                    const uint64_t lo = (r.s + (uint64_t)k * PassBytes<U>::value) & ~15ull;
+                    uint64_t hi = r.s + (uint64_t)(k + 1) * PassBytes<U>::value + 16u;
+                    if (hi > r.s + r.l)
+                        hi = r.s + r.l;
+                    prefetch_l2(lo, (uint32_t)(((hi + 15u) & ~15ull) - lo));
+                }
                 pdl_wait();
                 waited = true;
             }
@@ -899,21 +923,22 @@ cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), int ctas, int threads, 
 
 template <int U, int P>
 cudaError_t launch_ldg(bool pdl, int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
-                       unsigned long long *ctr, bool matched, unsigned *err, cudaStream_t s)
+                       unsigned long long *ctr, bool matched, unsigned *err, uint32_t flags, cudaStream_t s)
 {
     if (matched)
-        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, true>, ctas, threads, 0, s, t, n, passes, ctr, err);
-    return launch_k(pdl, kvx_copy_ldg_kernel<U, P, false>, ctas, threads, 0, s, t, n, passes, ctr, err);
+        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, true>, ctas, threads, 0, s, t, n, passes, ctr, err, flags);
+    return launch_k(pdl, kvx_copy_ldg_kernel<U, P, false>, ctas, threads, 0, s, t, n, passes, ctr, err, flags);
 }
 
 template <int U>
 cudaError_t launch_ldg_p(const Launch &l, int ctas, const kvx_chunk *t, uint32_t n,
                          uint32_t passes, unsigned long long *ctr, unsigned *err, cudaStream_t s)
 {
+    const uint32_t flags = (l.prefetch && ctr == nullptr) ? kLdgPrefetch : 0u;
     switch (l.store_policy) {
-    case 1: return launch_ldg<U, 1>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
-    case 2: return launch_ldg<U, 2>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
-    default: return launch_ldg<U, 0>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, s);
+    case 1: return launch_ldg<U, 1>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
+    case 2: return launch_ldg<U, 2>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
+    default: return launch_ldg<U, 0>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
     }
 }
 
