@@ -82,6 +82,7 @@ struct TableRow {
     uint64_t max_mean_chunk;  // row applies when mean chunk bytes <= this
     kvx_launch cfg;
     uint64_t min_payload = 0;  // ... and the batch carries at least this many bytes
+    bool unmatched_only = false;  // ... and (when set) some chunk's src and dst differ mod 16
 };
 
 struct EnvSettings {
@@ -96,11 +97,13 @@ struct EnvSettings {
 };
 
 // A launch table in a text file: one row per line, `#` starts a comment:
-//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy [assign [min_payload_bytes]]
+//   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy
+//       [assign [min_payload_bytes [phase]]]
 // with dir h2d|d2h|d2d, max_mean_chunk_bytes an integer or "inf", variant
-// ldg|bulk, assign static|dynamic|auto (absent or auto: the built-in choice
-// for dir), min_payload_bytes an integer (absent: 0). Rows are tried in file
-// order, before the built-in rows.
+// ldg|bulk|stage, assign static|dynamic|auto (absent or auto: the built-in
+// choice for dir), min_payload_bytes an integer (absent: 0), phase any|unmatched
+// (unmatched: only batches with a chunk whose src and dst differ mod 16; absent:
+// any). Rows are tried in file order, before the built-in rows.
 std::string parse_table(const char *path, std::vector<TableRow> *rows)
 {
     FILE *f = fopen(path, "r");
@@ -113,10 +116,10 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         ++lineno;
         if (char *h = strchr(line, '#'))
             *h = 0;
-        char dir[16], maxs[32], var[16], asg[16] = "", minp[32] = "";
+        char dir[16], maxs[32], var[16], asg[16] = "", minp[32] = "", phase[16] = "";
         int budget, threads, unroll, stages, policy;
-        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s %31s", dir, maxs, var, &budget, &threads,
-                               &unroll, &stages, &policy, asg, minp);
+        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s %31s %15s", dir, maxs, var, &budget,
+                               &threads, &unroll, &stages, &policy, asg, minp, phase);
         if (got <= 0)
             continue;  // blank or comment
         TableRow r{};
@@ -126,7 +129,12 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
             r.max_mean_chunk = ~0ull;
         else
             r.max_mean_chunk = strtoull(maxs, &end, 10);
-        const int variant = !strcmp(var, "ldg") ? KVX_VARIANT_LDG : !strcmp(var, "bulk") ? KVX_VARIANT_BULK : -1;
+        const int variant = !strcmp(var, "ldg")     ? KVX_VARIANT_LDG
+                            : !strcmp(var, "bulk")  ? KVX_VARIANT_BULK
+                            : !strcmp(var, "stage") ? KVX_VARIANT_STAGE
+                                                    : -1;
+        const int ph = (got < 11 || !strcmp(phase, "any")) ? 0 : !strcmp(phase, "unmatched") ? 1 : -1;
+        r.unmatched_only = ph == 1;
         const int assign = (got < 9 || !strcmp(asg, "auto")) ? KVX_ASSIGN_AUTO
                            : !strcmp(asg, "static") ? KVX_ASSIGN_STATIC
                            : !strcmp(asg, "dynamic") ? KVX_ASSIGN_DYNAMIC : -1;
@@ -136,10 +144,11 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         if (got < 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
             (threads != 128 && threads != 256 && threads != 512) || (unroll != 2 && unroll != 4 && unroll != 8) ||
             stages < 2 || stages > 12 || policy < 0 || policy > 2 || assign < 0 || (pend && *pend) ||
-            (got >= 10 && !isdigit((unsigned char)minp[0]))) {
+            (got >= 10 && !isdigit((unsigned char)minp[0])) || ph < 0 ||
+            (variant == KVX_VARIANT_STAGE && stages != 2 && stages != 4 && stages != 8)) {
             err = std::string("KVX_TABLE=") + path + ": line " + std::to_string(lineno) +
                   " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy "
-                  "[assign [min_payload]]'";
+                  "[assign [min_payload [phase]]]'";
             break;
         }
         r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy, assign};
@@ -166,8 +175,10 @@ const EnvSettings &env()
                 e.variant = KVX_VARIANT_LDG;
             else if (!strcmp(v, "bulk"))
                 e.variant = KVX_VARIANT_BULK;
+            else if (!strcmp(v, "stage"))
+                e.variant = KVX_VARIANT_STAGE;
             else
-                e.error = std::string("KVX_VARIANT=") + v + " is not auto, ldg or bulk";
+                e.error = std::string("KVX_VARIANT=") + v + " is not auto, ldg, bulk or stage";
         }
         if (const char *v = getenv("KVX_CTA_BUDGET")) {
             char *end = nullptr;
@@ -562,9 +573,19 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 0.971, 24 KiB x 21,845 (chunks of 16 and 8 KiB, which waste the ring's
 // stages) 0.974 against 0.934 for the ring, 16 KiB x 4,096 0.981 against
 // 0.894 for the ring, whose fill and drain do not amortise over 64 MiB.
+//
+// D2D batches of 128 MiB and more with a chunk whose source and destination
+// differ mod 16 (the LDG kernel then runs its re-pairing instance, 118
+// registers a thread) take the STAGE kernel: 4 warps a CTA, 4 stages of 4 KiB
+// per warp, 1,216 CTAs. Odd-tail cells (sizes 8 mod 16, either side shifted
+// by 8 bytes at random): 4 KiB x 65,536 0.916 against 0.877 for LDG, 8 KiB x
+// 65,536 0.936 against 0.898, 16 KiB x 32,768 0.948 against 0.921, 28 KiB x
+// 18,724 0.942 against 0.920. Smaller ones stay with LDG (16 KiB x 4,096 odd:
+// 0.890 LDG against 0.856), as do matched batches (phase-matched LDG: 0.97-0.99).
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 1216, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
@@ -583,7 +604,7 @@ struct BatchShape {
 bool row_matches(const TableRow &r, int dir, const BatchShape &b)
 {
     return r.dir == dir && b.mean_chunk <= r.max_mean_chunk && b.payload >= r.min_payload &&
-           (b.aligned || r.cfg.variant != KVX_VARIANT_BULK);
+           (b.aligned || r.cfg.variant != KVX_VARIANT_BULK) && (!r.unmatched_only || !b.matched);
 }
 
 // The row for a batch of this direction and shape.
@@ -636,8 +657,8 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     int policy = (want && want->store_policy) ? want->store_policy : t.store_policy;
     int assign = (want && want->assign) ? want->assign : t.assign;
     if (want) {
-        if (want->variant < 0 || want->variant > KVX_VARIANT_BULK)
-            return fail(KVX_ERR_INVALID_ARG, "variant %d is not AUTO, LDG or BULK", want->variant);
+        if (want->variant < 0 || want->variant > KVX_VARIANT_STAGE)
+            return fail(KVX_ERR_INVALID_ARG, "variant %d is not AUTO, LDG, BULK or STAGE", want->variant);
         if (want->cta_budget < 0)
             return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", want->cta_budget);
         if (want->threads && want->threads != 128 && want->threads != 256 && want->threads != 512)
@@ -653,6 +674,11 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     }
     if (variant == KVX_VARIANT_AUTO)
         variant = t.variant;
+    if (variant == KVX_VARIANT_STAGE && stages != 2 && stages != 4 && stages != 8) {
+        if (want && want->stages)
+            return fail(KVX_ERR_INVALID_ARG, "stages %d is not 2, 4 or 8 for the STAGE variant", want->stages);
+        stages = 4;  // the table row was another variant's
+    }
     out->variant = variant;
     out->ctas = budget;
     out->threads = threads;
@@ -1149,6 +1175,7 @@ kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *ou
         return fail(KVX_ERR_INVALID_ARG, "null output");
     BatchShape b;
     b.mean_chunk = mean_chunk_bytes;
+    b.matched = true;  // 16-byte aligned descriptors
     *out = table_launch(dir, b);
     return KVX_OK;
 }
@@ -1170,13 +1197,13 @@ kvx_status kvx_select_launch(const uint64_t *src, const uint64_t *dst, const uin
     st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), want, &l);
     if (st != KVX_OK)
         return st;
-    const bool ldg = l.variant == KVX_VARIANT_LDG;
+    const bool ldg = l.variant == KVX_VARIANT_LDG, stage = l.variant == KVX_VARIANT_STAGE;
     *out = kvx_launch{l.variant,
                       chunks ? kvx::work_ctas(l, (uint32_t)chunks, max_chunk) : 0,
-                      ldg ? l.threads : 0,
+                      ldg ? l.threads : stage ? 128 : 0,
                       ldg ? l.unroll : 0,
                       ldg ? 0 : l.stages,
-                      ldg ? l.store_policy : 0,
+                      (ldg || stage) ? l.store_policy : 0,
                       ldg ? (kvx::ldg_dynamic(l, (uint32_t)chunks, max_chunk) ? KVX_ASSIGN_DYNAMIC
                                                                              : KVX_ASSIGN_STATIC)
                           : 0};
@@ -1349,7 +1376,7 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
         return st;
     kvx_launch merged = b->selected;
     if (want) {
-        if (want->variant < 0 || want->variant > KVX_VARIANT_BULK || want->cta_budget < 0)
+        if (want->variant < 0 || want->variant > KVX_VARIANT_STAGE || want->cta_budget < 0)
             return fail(KVX_ERR_INVALID_ARG, "bad variant %d or cta_budget %d", want->variant,
                         want->cta_budget);
         if (want->variant)
@@ -1366,6 +1393,10 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
             merged.store_policy = want->store_policy;
         if (want->assign)
             merged.assign = want->assign;
+        // another variant's ring size is not a request for the STAGE ring
+        if (want->variant == KVX_VARIANT_STAGE && b->selected.variant != KVX_VARIANT_STAGE && !want->stages &&
+            merged.stages != 2 && merged.stages != 4 && merged.stages != 8)
+            merged.stages = 0;
     }
     Launch l;
     st = resolve(b->dir, BatchShape{}, &merged, &l);
@@ -1512,7 +1543,9 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     // row for the direction (its small-chunk row) and apply the caller's fields.
     if (want && want->variant && want->variant != KVX_VARIANT_LDG)
         return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
-    kvx_launch merged = table_launch(dir, BatchShape{});
+    BatchShape list_shape;
+    list_shape.matched = true;  // not a STAGE row: the list's phases are not known on the host
+    kvx_launch merged = table_launch(dir, list_shape);
     if (want) {
         if (want->cta_budget < 0)
             return fail(KVX_ERR_INVALID_ARG, "cta_budget %d < 0", want->cta_budget);

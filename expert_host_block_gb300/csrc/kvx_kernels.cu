@@ -1,10 +1,10 @@
 // Copy kernels of kvx for sm_103a.
 //
-// Both variants walk the same table of 32-byte chunk records ({src, dst,
+// The variants walk the same table of 32-byte chunk records ({src, dst,
 // len <= 16 KiB, desc}, after a header record) as a persistent grid: work
 // unit u goes to worker (u mod workers), where a worker is a warp (LDG, whose
-// units are warp passes of at most 512 * U bytes) or a CTA (BULK, whose units
-// are chunks). Units are small and of nearly equal size, so handing them out
+// units are warp passes of at most 512 * U bytes; STAGE, whose units are 4 KiB
+// passes) or a CTA (BULK, whose units are chunks). Units are small and of nearly equal size, so handing them out
 // round-robin spreads the batch's bytes evenly over the workers, whatever mix
 // of descriptor sizes it holds (FreeToken issue #751, §Problem in upstream
 // today and §What we changed: split the call's bytes, not its banks, over the
@@ -26,6 +26,11 @@
 // form). Here a stage is as large as the batch's longest chunk, so a ring of
 // 4 KiB chunks has many more stages, and loads, in flight than one of 16 KiB
 // chunks. Every mbarrier wait is bounded by %globaltimer.
+//
+// STAGE variant: every warp has its own ring of 4 KiB stages; lane 0 bulk-loads
+// the 16-byte blocks holding each unit, the whole warp stores the unit with
+// 16-byte stores at the destination's phase. Loads in flight cost shared
+// memory instead of registers, which pays off when phases differ.
 //
 // Unaligned pieces: addresses and sizes are multiples of 8. When src and dst
 // have the same phase mod 16, a chunk is an 8-byte head, a 16-byte-word body
@@ -680,6 +685,202 @@ __global__ void __launch_bounds__(32) kvx_copy_bulk_kernel(const kvx_chunk *__re
     __syncwarp();
 }
 
+// ---- STAGE variant ----------------------------------------------------------
+//
+// For batches whose chunks' sources and destinations do not agree mod 16 the
+// LDG kernel must re-pair 16-byte words across lanes, which costs registers
+// (118 a thread: 16 warps per SM) and therefore bytes in flight. Here one lane
+// of each warp bulk-loads the 16-byte blocks holding a unit (cp.async.bulk into
+// shared::cta, completed on an mbarrier) into a ring of S stages of its own,
+// and the whole warp stores the unit from there with 16-byte st.global, reading
+// shared memory at whatever 8-byte phase the destination needs. No register
+// holds a load in flight, so a warp keeps S units (S x 4 KiB) in flight with
+// ~45 registers. Units are warp passes of at most kStageUnit bytes, handed out
+// by position as in the LDG kernel; waits are bounded as in the BULK kernel.
+
+constexpr uint32_t kStageUnit = 4096;             // payload bytes per unit
+constexpr uint32_t kStageBytes = kStageUnit + 32; // a unit's 16-byte blocks fit in kStageUnit + 16
+constexpr int kStageWarps = 4;                    // warps per CTA (128 threads)
+
+// One unit: its source, destination and length (0: the chunk has no such pass).
+struct URec {
+    uint64_t s, d;
+    uint32_t l;
+};
+
+__device__ __forceinline__ URec stage_unit(const kvx_chunk *__restrict__ tab, uint64_t u, uint32_t n_chunks,
+                                           unsigned *err)
+{
+    const uint64_t pass = u / n_chunks;
+    const Rec r = load_rec(tab, u - pass * n_chunks, err);
+    URec o{0, 0, 0};
+    const uint64_t off = pass * kStageUnit;
+    if (off < r.l) {
+        o.s = r.s + off;
+        o.d = r.d + off;
+        o.l = (uint32_t)(r.l - off < kStageUnit ? r.l - off : kStageUnit);
+    }
+    return o;
+}
+
+__device__ __forceinline__ URec shfl_unit(const URec &r, int src_lane)
+{
+    URec o;
+    o.s = __shfl_sync(kFull, r.s, src_lane);
+    o.d = __shfl_sync(kFull, r.d, src_lane);
+    o.l = __shfl_sync(kFull, r.l, src_lane);
+    return o;
+}
+
+__device__ __forceinline__ uint2 lds8(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+// Order this thread's earlier shared-memory accesses before later bulk copies
+// (the async proxy) that write the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Store unit `u` from the stage at shared address `st`, whose byte 0 is the
+// global byte (u.s & ~15). Lane 0 writes the 8-byte head that brings the
+// destination to 16-byte alignment, all lanes the 16-byte body words, lane 1
+// the 8-byte tail.
+template <int P>
+__device__ __forceinline__ void stage_store(const URec &u, uint32_t st, uint32_t lane)
+{
+    const uint32_t o = (uint32_t)(u.s & 15u);   // 0 or 8: where the unit's first byte sits in the stage
+    const uint32_t hd = (u.d & 15u) ? 8u : 0u;  // len >= 8 whenever hd != 0
+    if (hd && lane == 0)
+        st8<P>(reinterpret_cast<unsigned char *>(u.d), lds8(st + o));
+    const uint32_t ob = o + hd;
+    const uint64_t db = u.d + hd;
+    const uint32_t blen = u.l - hd;
+    const uint32_t nb = blen >> 4;
+    if (ob & 15u) {
+        for (uint32_t j = lane; j < nb; j += 32u) {
+            const uint2 a = lds8(st + ob + 16u * j), b = lds8(st + ob + 16u * j + 8u);
+            st16<P>(reinterpret_cast<unsigned char *>(db + 16ull * j), make_uint4(a.x, a.y, b.x, b.y));
+        }
+    } else {
+        for (uint32_t j = lane; j < nb; j += 32u)
+            st16<P>(reinterpret_cast<unsigned char *>(db + 16ull * j), lds16(st + ob + 16u * j));
+    }
+    if ((blen & 15u) && lane == 1)
+        st8<P>(reinterpret_cast<unsigned char *>(db + 16ull * nb), lds8(st + ob + 16u * nb));
+}
+
+// Warp w copies its units k = 0, 1, ... (unit w + k x warps): lane 0 keeps the
+// loads of units k + 1 .. k + S - 1 in flight while the warp stores unit k. The
+// records of the warp's units [a0, a0 + 64) sit in two registers per lane (unit
+// a0 + i in lane i of wa, a0 + 32 + i of wb), loaded 32 at a time; the
+// look-ahead k + S stays below a0 + 64 because S <= 32.
+template <int S, int P>
+__global__ void __launch_bounds__(kStageWarps * 32) kvx_copy_stage_kernel(const kvx_chunk *__restrict__ tab,
+                                                                         uint32_t n_chunks, uint32_t passes,
+                                                                         uint64_t wait_ns, unsigned *err)
+{
+    static_assert(S >= 2 && S <= 32, "stages per warp");
+    extern __shared__ __align__(128) unsigned char stage_ring[];
+    __shared__ __align__(8) uint64_t bars[kStageWarps][S];
+    pdl_trigger();
+    const uint32_t lane = threadIdx.x & 31u, wib = threadIdx.x >> 5;
+    const uint32_t ring0 = smem_u32(stage_ring) + wib * (uint32_t)S * kStageBytes;
+    const uint32_t bar0 = smem_u32(&bars[wib][0]);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s)
+            mbar_init(bar0 + 8u * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const uint64_t gwarp = (uint64_t)blockIdx.x * kStageWarps + wib;
+    const uint64_t nwarps = (uint64_t)gridDim.x * kStageWarps;
+    const uint64_t n_units = (uint64_t)n_chunks * passes;
+    const uint64_t my_n = n_units > gwarp ? (n_units - 1 - gwarp) / nwarps + 1 : 0;
+    auto rec_k = [&](uint64_t k) {
+        URec r{0, 0, 0};
+        if (k < my_n)
+            r = stage_unit(tab, gwarp + k * nwarps, n_chunks, err);
+        return r;
+    };
+    uint64_t a0 = 0;
+    URec wa = rec_k(lane), wb = rec_k(32u + lane);
+    pdl_wait();  // records only before this point
+    auto get = [&](uint64_t k) {  // the warp's unit k, k in [a0, a0 + 64); every lane takes part
+        const uint64_t o = k - a0;
+        const URec x = shfl_unit(wa, (int)(o & 31u)), y = shfl_unit(wb, (int)(o & 31u));
+        return o < 32u ? x : y;
+    };
+    auto issue = [&](const URec &u, uint32_t s) {  // lane 0: load the 16-byte blocks holding u into stage s
+        const uint64_t lo = u.s & ~15ull;
+        const uint32_t bytes = (uint32_t)(((u.s + u.l + 15u) & ~15ull) - lo);  // <= kStageUnit + 16
+        mbar_arrive_expect_tx(bar0 + 8u * s, bytes);
+        bulk_load(ring0 + s * kStageBytes, lo, bytes, bar0 + 8u * s);
+    };
+    uint32_t phase = 0;    // bit s: parity of the next completion of stage s
+    uint32_t pending = 0;  // bit s: a load is in flight on stage s
+    bool timed_out = false;
+    for (uint32_t j = 0; j < (uint32_t)S && j < my_n; ++j) {
+        const URec u = get(j);
+        if (u.l) {
+            if (lane == 0)
+                issue(u, j);
+            pending |= 1u << j;
+        }
+    }
+    uint32_t st = 0;  // stage of unit k: k mod S
+    for (uint64_t k = 0; k < my_n; ++k) {
+        if (k == a0 + 32) {
+            wa = wb;
+            wb = rec_k(a0 + 64 + lane);
+            a0 += 32;
+        }
+        const URec u = get(k);
+        if (u.l) {
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait_bounded(bar0 + 8u * st, (phase >> st) & 1u, wait_ns);
+            if (!__shfl_sync(kFull, (int)ok, 0)) {
+                timed_out = true;
+                break;
+            }
+            phase ^= 1u << st;
+            pending &= ~(1u << st);
+            stage_store<P>(u, ring0 + st * kStageBytes, lane);
+        }
+        const uint64_t kn = k + S;
+        const URec un = kn < my_n ? get(kn) : URec{0, 0, 0};
+        __syncwarp();  // every lane has read stage st
+        if (un.l) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(un, st);
+            }
+            pending |= 1u << st;
+        }
+        st = st + 1 == (uint32_t)S ? 0 : st + 1;
+    }
+    if (timed_out && lane == 0) {
+        report(err, kDevErrTimeout);
+        // let the loads still in flight land before the shared memory goes away
+        for (int s = 0; s < S; ++s)
+            if (pending & (1u << s))
+                mbar_wait_bounded(bar0 + 8u * s, (phase >> s) & 1u, wait_ns);
+    }
+    __syncwarp();
+}
+
 // ---- descriptors that live on the device -------------------------------------
 //
 // A producer kernel (a MoE router, a block manager on the GPU) writes the
@@ -959,6 +1160,30 @@ cudaError_t launch_bulk(bool pdl, int ctas, int ring_units, const kvx_chunk *t, 
     return launch_k(pdl, kvx_copy_bulk_kernel, ctas, 32, ring, s, t, n, stage, S, kBulkWaitNs, err);
 }
 
+template <int S, int P>
+cudaError_t launch_stage_sp(bool pdl, int ctas, const kvx_chunk *t, uint32_t n, uint32_t passes, unsigned *err,
+                            cudaStream_t s)
+{
+    const size_t smem = (size_t)kStageWarps * S * kStageBytes;
+    cudaError_t e = cudaFuncSetAttribute(kvx_copy_stage_kernel<S, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_k(pdl, kvx_copy_stage_kernel<S, P>, ctas, kStageWarps * 32, smem, s, t, n, passes, kBulkWaitNs,
+                    err);
+}
+
+template <int S>
+cudaError_t launch_stage_s(const Launch &l, int ctas, const kvx_chunk *t, uint32_t n, uint32_t passes, unsigned *err,
+                           cudaStream_t s)
+{
+    switch (l.store_policy) {
+    case 1: return launch_stage_sp<S, 1>(l.pdl, ctas, t, n, passes, err, s);
+    case 2: return launch_stage_sp<S, 2>(l.pdl, ctas, t, n, passes, err, s);
+    default: return launch_stage_sp<S, 0>(l.pdl, ctas, t, n, passes, err, s);
+    }
+}
+
 template <int U>
 cudaError_t launch_devlist_p(const Launch &l, const uint64_t *src, const uint64_t *dst,
                             const uint64_t *sizes, DevListMeta *meta, const uint64_t *offsets, bool dyn,
@@ -974,6 +1199,12 @@ cudaError_t launch_devlist_p(const Launch &l, const uint64_t *src, const uint64_
 }  // namespace
 
 size_t bulk_smem_bytes(int stages) { return (size_t)stages * KVX_CHUNK_BYTES; }
+
+uint32_t stage_passes(uint32_t max_chunk_len)
+{
+    const uint32_t p = (max_chunk_len + kStageUnit - 1) / kStageUnit;
+    return p ? p : 1u;
+}
 
 uint32_t ldg_passes(const Launch &l, uint32_t max_chunk_len)
 {
@@ -998,6 +1229,8 @@ int work_ctas(const Launch &l, uint32_t n_chunks, uint32_t max_chunk_len)
     uint64_t need;
     if (l.variant == KVX_VARIANT_BULK) {
         need = n_chunks;
+    } else if (l.variant == KVX_VARIANT_STAGE) {
+        need = ((uint64_t)n_chunks * stage_passes(max_chunk_len) + kStageWarps - 1) / kStageWarps;
     } else {
         const uint64_t units = (uint64_t)n_chunks * ldg_passes(l, max_chunk_len);
         need = (units + (uint64_t)(l.threads / 32) - 1) / (uint64_t)(l.threads / 32);
@@ -1016,6 +1249,14 @@ cudaError_t launch_copy(const Launch &l, kvx_chunk *table, uint32_t n_chunks,
     const kvx_chunk *recs = table + kTableHeader;
     if (l.variant == KVX_VARIANT_BULK) {
         return launch_bulk(l.pdl, ctas, l.stages, recs, n_chunks, max_chunk_len, err, stream);
+    }
+    if (l.variant == KVX_VARIANT_STAGE) {
+        const uint32_t passes = stage_passes(max_chunk_len);
+        switch (l.stages) {
+        case 2: return launch_stage_s<2>(l, ctas, recs, n_chunks, passes, err, stream);
+        case 8: return launch_stage_s<8>(l, ctas, recs, n_chunks, passes, err, stream);
+        default: return launch_stage_s<4>(l, ctas, recs, n_chunks, passes, err, stream);
+        }
     }
     const uint32_t passes = ldg_passes(l, max_chunk_len);
     unsigned long long *ctr =

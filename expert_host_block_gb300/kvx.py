@@ -25,8 +25,9 @@ LIB_PATH = _build.LIB_PATH
 
 KVX_H2D, KVX_D2H, KVX_D2D = 0, 1, 2
 DIRS = {"h2d": KVX_H2D, "d2h": KVX_D2H, "d2d": KVX_D2D}
-KVX_VARIANT_AUTO, KVX_VARIANT_LDG, KVX_VARIANT_BULK = 0, 1, 2
-VARIANTS = {"auto": KVX_VARIANT_AUTO, "ldg": KVX_VARIANT_LDG, "bulk": KVX_VARIANT_BULK}
+KVX_VARIANT_AUTO, KVX_VARIANT_LDG, KVX_VARIANT_BULK, KVX_VARIANT_STAGE = 0, 1, 2, 3
+VARIANTS = {"auto": KVX_VARIANT_AUTO, "ldg": KVX_VARIANT_LDG, "bulk": KVX_VARIANT_BULK,
+            "stage": KVX_VARIANT_STAGE}
 KVX_ASSIGN_AUTO, KVX_ASSIGN_STATIC, KVX_ASSIGN_DYNAMIC = 0, 1, 2
 ASSIGNS = {"auto": KVX_ASSIGN_AUTO, "static": KVX_ASSIGN_STATIC, "dynamic": KVX_ASSIGN_DYNAMIC}
 

@@ -90,7 +90,10 @@ typedef enum kvx_dir {
 typedef enum kvx_variant {
     KVX_VARIANT_AUTO = 0, /* pick from the calibrated table by direction and size */
     KVX_VARIANT_LDG = 1,  /* 16-byte loads/stores by every lane, several in flight */
-    KVX_VARIANT_BULK = 2  /* cp.async.bulk through a shared::cta ring, one issuing lane */
+    KVX_VARIANT_BULK = 2, /* cp.async.bulk through a shared::cta ring, one issuing lane */
+    KVX_VARIANT_STAGE = 3 /* cp.async.bulk loads into a shared::cta ring per warp, 16-byte stores by the
+                             whole warp at any 8-byte phase (128 threads a CTA): for batches whose
+                             sources and destinations do not agree mod 16 */
 } kvx_variant;
 
 /* How the LDG kernel hands work units (one warp pass over a chunk) to warps. */
@@ -135,7 +138,8 @@ typedef struct kvx_launch {
     int threads;         /* LDG: threads per CTA, one of 128, 256, 512 */
     int unroll;          /* LDG: 16-byte loads in flight per lane, one of 2, 4, 8 */
     int stages;          /* BULK: shared-memory ring of stages x KVX_CHUNK_BYTES, 2..12; it is cut
-                            into stages of the batch's longest chunk (at most 32 stages) */
+                            into stages of the batch's longest chunk (at most 32 stages).
+                            STAGE: 4 KiB units each warp keeps in flight, 2, 4 or 8 */
     int store_policy;    /* LDG: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
     int assign;          /* LDG: kvx_assign */
 } kvx_launch;
@@ -358,8 +362,10 @@ kvx_status kvx_select_launch(const uint64_t *src_addrs, const uint64_t *dst_addr
  * direction, mean chunk size and, for some rows, the batch's payload (the D2D
  * bulk row needs 256 MiB or more). A row that selects KVX_VARIANT_BULK applies
  * only to batches with at least 90 % of their bytes in descriptors whose
- * source, destination and size are multiples of 16; other batches take the
- * next matching row. */
+ * source, destination and size are multiples of 16; the D2D row that selects
+ * KVX_VARIANT_STAGE only to batches of 128 MiB or more with a chunk whose
+ * source and destination differ mod 16; other batches take the next matching
+ * row. */
 kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *out);
 
 /* Process-wide validation level for kvx_copy_batch / kvx_upload_descriptors

@@ -265,7 +265,8 @@ def test_copy_batch_rejects_before_any_cuda_call():
 
 
 @pytest.mark.parametrize("launch", [
-    {"variant": 3}, {"threads": 1024}, {"threads": 96}, {"unroll": 3}, {"stages": 13},
+    {"variant": 4}, {"variant": "stage", "stages": 6}, {"threads": 1024}, {"threads": 96}, {"unroll": 3},
+    {"stages": 13},
     {"store_policy": 3}, {"cta_budget": -2}, {"assign": 3}, {"assign": -1},
 ])
 def test_copy_batch_ex_rejects_bad_launch(launch):
@@ -382,7 +383,8 @@ def test_kvx_table_file_overrides_rows(tmp_path):
                      "h2d 8192 bulk 7 256 8 5 0\n"
                      "h2d inf ldg 33 512 4 3 1 static\n"
                      "d2d inf bulk 11 256 8 4 0 auto 1099511627776\n"  # batches of 1 TiB and more
-                     "d2d inf ldg 99 512 8 3 0 dynamic\n")
+                     "d2d inf ldg 99 512 8 3 0 dynamic\n"
+                     "d2h inf stage 21 128 8 2 0 auto 0 unmatched\n")
     code = ("from expert_host_block_gb300 import kvx\n"
             "print(kvx.kvx_default_launch('h2d', 4096))\n"
             "print(kvx.kvx_default_launch('h2d', 16384))\n"
@@ -396,11 +398,23 @@ def test_kvx_table_file_overrides_rows(tmp_path):
     assert "'variant': 1, 'cta_budget': 64" in lines[2]  # no d2h row in the file: built-in row
     # kvx_default_launch describes a large batch: the 1 TiB row applies (assign auto: static for d2d)
     assert "'variant': 2, 'cta_budget': 11" in lines[3] and "'assign': 1" in lines[3]
+    # the phase column: the d2h stage row applies only to batches whose phases differ
+    code2 = ("import numpy as np\n"
+             "from expert_host_block_gb300 import kvx\n"
+             "i = np.arange(64, dtype=np.uint64)\n"
+             "s = np.uint64(1 << 36) + i * np.uint64(8192)\n"
+             "d = np.uint64(1 << 32) + i * np.uint64(8192)\n"
+             "z = np.full(64, 4096, dtype=np.uint64)\n"
+             "print(kvx.kvx_select_launch(s, d, z, None, 'd2h')['variant'])\n"
+             "print(kvx.kvx_select_launch(s + np.uint64(8), d, z, None, 'd2h')['variant'])\n")
+    out = _run_with_env(code2, KVX_TABLE=str(table))
+    assert out.stdout.split() == ["1", "3"], out.stdout + out.stderr
 
 
 @pytest.mark.parametrize("text", ["h2d 4096 tma 8 256 8 3 0\n", "h2d 4096 ldg 8 300 8 3 0\n",
                                   "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n",
-                                  "h2d inf ldg 8 256 8 3 0 greedy\n", "h2d inf ldg 8 256 8 3 0 auto 12x\n"])
+                                  "h2d inf ldg 8 256 8 3 0 greedy\n", "h2d inf ldg 8 256 8 3 0 auto 12x\n",
+                                  "d2d inf stage 8 128 8 3 0\n", "d2d inf ldg 8 256 8 3 0 auto 0 odd\n"])
 def test_kvx_table_malformed_is_an_error(tmp_path, text):
     table = tmp_path / "bad.table"
     table.write_text(text)
@@ -461,13 +475,15 @@ def test_select_launch_d2d_rows_follow_payload_and_alignment():
     assert below["variant"] == kvx.KVX_VARIANT_LDG and below["threads"] == 128
     # chunks of 16 and 8 KiB (mean 12 KiB) stay with LDG at any payload
     assert kvx.kvx_select_launch(*_batch(16384, 24576), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
-    odd = kvx.kvx_select_launch(*_batch(16384, 16384, slot=32768, src_phase=8), None, "d2d")
-    assert odd["variant"] == kvx.KVX_VARIANT_LDG
-    # 9 % of the bytes misaligned still takes the ring; 11 % does not
+    odd = kvx.kvx_select_launch(*_batch(4096, 16384, slot=32768, src_phase=8), None, "d2d")
+    assert odd["variant"] == kvx.KVX_VARIANT_LDG  # 64 MiB with phases that differ: below the STAGE row
+    # 9 % of the bytes misaligned (source and destination shifted alike) still takes the ring; 11 % does not
     s, d, z = _batch(20000, 16384, slot=32768)
     s[:1800] += 8
+    d[:1800] += 8
     assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_BULK
     s[:2200] = s[:2200] | 8
+    d[:2200] = d[:2200] | 8
     assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
     # small chunks stay with LDG at any payload
     assert kvx.kvx_select_launch(*_batch(65536, 4096), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
@@ -476,6 +492,31 @@ def test_select_launch_d2d_rows_follow_payload_and_alignment():
     assert forced["variant"] == kvx.KVX_VARIANT_BULK
     forced = kvx.kvx_select_launch(*_batch(16384, 4096), None, "h2d", {"assign": "static", "cta_budget": 7})
     assert forced["assign"] == kvx.KVX_ASSIGN_STATIC and forced["cta_budget"] == 7
+
+
+def test_select_launch_stage_row_for_mismatched_phases():
+    # D2D batches of 128 MiB or more with a chunk whose source and destination differ mod 16
+    l = kvx.kvx_select_launch(*_batch(65536, 4096, slot=8192, src_phase=8), None, "d2d")
+    assert (l["variant"], l["threads"], l["unroll"], l["stages"]) == (kvx.KVX_VARIANT_STAGE, 128, 0, 4)
+    assert l["cta_budget"] == 1216 and l["assign"] == 0
+    # one mismatched chunk is enough; 16-byte phases that agree are not
+    s, d, z = _batch(32768, 8192, slot=16384)
+    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    s[7] += 8
+    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_STAGE
+    # below 128 MiB, and over the host link, LDG
+    assert kvx.kvx_select_launch(*_batch(16383, 8192, slot=16384, src_phase=8), None,
+                                 "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    assert kvx.kvx_select_launch(*_batch(65536, 4096, slot=8192, src_phase=8), None,
+                                 "h2d")["variant"] == kvx.KVX_VARIANT_LDG
+    # asked for: the grid follows 4 warps a CTA, one 4 KiB unit each per pass; stages 2, 4 or 8 only
+    l = kvx.kvx_select_launch(*_batch(100, 16384), None, "h2d", {"variant": "stage", "stages": 8, "cta_budget": 999})
+    assert (l["variant"], l["cta_budget"], l["stages"]) == (kvx.KVX_VARIANT_STAGE, 100, 8)
+    l = kvx.kvx_select_launch(*_batch(100, 16384), None, "h2d", {"variant": "stage"})
+    assert l["stages"] == 4  # the h2d row's stages belong to another variant
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_select_launch(*_batch(100, 16384), None, "h2d", {"variant": "stage", "stages": 3})
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
 
 
 def test_select_launch_rejects_what_copy_batch_rejects():

@@ -43,12 +43,14 @@ def _random_case(seed, matched=False):
     dst = (g.permutation(n_slots)[:n] * slot + dst_phase).astype(np.uint64)
     src = (g.integers(0, n_slots, n) * slot + src_phase).astype(np.uint64)  # may repeat
     body = n_slots * slot
-    launch = {"variant": str(g.choice(["ldg", "bulk"])), "cta_budget": int(g.choice([1, 3, 16, 64, 300]))}
+    launch = {"variant": str(g.choice(["ldg", "bulk", "stage"])), "cta_budget": int(g.choice([1, 3, 16, 64, 300]))}
     if launch["variant"] == "ldg":
         launch.update(threads=int(g.choice([128, 256, 512])), unroll=int(g.choice([2, 4, 8])),
                       store_policy=int(g.integers(0, 3)), assign=int(g.integers(0, 3)))
-    else:
+    elif launch["variant"] == "bulk":
         launch["stages"] = int(g.integers(2, 13))
+    else:
+        launch.update(stages=int(g.choice([2, 4, 8])), store_policy=int(g.integers(0, 3)))
     ws = "host" if direction == "h2d" else "device"
     wd = "host" if direction == "d2h" else "device"
     specs = {"src": W.PoolSpec("src", ws, body, "random", (77, seed)),

@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 LDG = {"variant": "ldg"}
 BULK = {"variant": "bulk"}
+STAGE = {"variant": "stage"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,7 +54,10 @@ def _one(pools, batch, **kw):
                                     {"variant": "bulk", "cta_budget": 32, "stages": 2},
                                     {"variant": "bulk", "cta_budget": 8, "stages": 4},
                                     {"variant": "bulk", "cta_budget": 4, "stages": 12},
-                                    {"variant": "bulk", "cta_budget": 1, "stages": 7}])
+                                    {"variant": "bulk", "cta_budget": 1, "stages": 7},
+                                    STAGE,
+                                    {"variant": "stage", "cta_budget": 1, "stages": 2},
+                                    {"variant": "stage", "cta_budget": 3, "stages": 8}])
 def test_tiny_h2d(launch):
     w = W.tiny_h2d()
     p = Pools(w.pools)
@@ -78,7 +82,7 @@ def test_ldg_launch_shapes(threads, unroll, policy):
 
 # ---- config: KV burst, 16,384 x 4 KiB per direction, H2D || D2H, full size ---
 
-@pytest.mark.parametrize("launch", [None, BULK])
+@pytest.mark.parametrize("launch", [None, BULK, STAGE])
 def test_kv_burst_bidirectional(launch):
     w = W.kv_burst(n_sets=1)
     p = Pools(w.pools)
@@ -152,7 +156,7 @@ def test_kv_burst_many_sets_ring_reuse():
 @pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
 @pytest.mark.parametrize("odd", [False, True])
 @pytest.mark.parametrize("size_kib", W.SWEEP_SIZES_KIB)
-@pytest.mark.parametrize("launch", [LDG, BULK])
+@pytest.mark.parametrize("launch", [LDG, BULK, STAGE])
 def test_sweep_cells(direction, odd, size_kib, launch):
     w = W.sweep_cell(size_kib, 256, direction, odd_tails=odd)
     p = Pools(w.pools)
@@ -186,7 +190,7 @@ def test_sweep_full_size_cell(direction):
 
 # ---- config: MoE expert-miss gather, full size -----------------------------------
 
-@pytest.mark.parametrize("launch", [None, LDG, BULK])
+@pytest.mark.parametrize("launch", [None, LDG, BULK, STAGE])
 def test_moe_gather(launch):
     m = W.MoeGather()
     p = Pools(m.pools)
@@ -214,7 +218,7 @@ def _batch(so, do, sz, direction):
     return W.Batch("src", "dst", u(so), u(do), u(sz), direction)
 
 
-@pytest.mark.parametrize("launch", [LDG, BULK])
+@pytest.mark.parametrize("launch", [LDG, BULK, STAGE])
 @pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
 def test_phase_combinations(direction, launch):
     """Sizes 8..40 and around the chunk size at every (src mod 16, dst mod 16) pair."""
@@ -250,7 +254,7 @@ def test_empty_and_zero_size_batches():
         p.close()
 
 
-@pytest.mark.parametrize("launch", [LDG, BULK])
+@pytest.mark.parametrize("launch", [LDG, BULK, STAGE])
 def test_single_large_descriptor(launch):
     """One 64 MiB descriptor (4,096 chunks) and one 8-byte descriptor."""
     p = _pools_small("device", "device", body=80 * W.MIB)
@@ -272,7 +276,7 @@ def test_same_pool_d2d():
 
 # ---- descriptor buffers, graph capture ---------------------------------------------
 
-@pytest.mark.parametrize("variant", ["ldg", "bulk"])
+@pytest.mark.parametrize("variant", ["ldg", "bulk", "stage"])
 def test_desc_buf_upload_and_replay(variant):
     w = W.kv_burst(n_sets=2, n_per_dir=4096, pool_bytes=128 * W.MIB)
     p = Pools(w.pools)
@@ -546,6 +550,21 @@ def test_bulk_ring_sizes_with_mixed_alignment(stages, size_kib):
         p.close()
 
 
+@pytest.mark.parametrize("direction", ["h2d", "d2h", "d2d"])
+@pytest.mark.parametrize("stages", [2, 4, 8])
+@pytest.mark.parametrize("budget,policy", [(1, 0), (5, 1), (1216, 2)])
+def test_stage_launch_shapes(direction, stages, budget, policy):
+    """The STAGE kernel at every ring depth, a few grids and every store policy, on odd-tail chunks of up to
+    28 KiB (two chunks each: 16 KiB + the rest, seven 4 KiB units), every phase pair."""
+    w = W.sweep_cell(28, 300, direction, odd_tails=True)
+    p = Pools(w.pools)
+    try:
+        _one(p, w.batches[0], launch={"variant": "stage", "stages": stages, "cta_budget": budget,
+                                      "store_policy": policy})
+    finally:
+        p.close()
+
+
 def test_status_tokens_pipelined():
     """Submit, enqueue a status read, submit more, then collect: the enqueue-only pattern."""
     w = W.kv_burst(n_sets=4, n_per_dir=2048, pool_bytes=64 * W.MIB)
@@ -600,10 +619,12 @@ def test_status_token_pending_then_timeout_then_expiry():
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("n,odd,variant", [(4096, False, "ldg"), (32768, False, "bulk"), (32768, True, "ldg")])
+@pytest.mark.parametrize("n,odd,variant", [(4096, False, "ldg"), (32768, False, "bulk"), (32768, True, "stage"),
+                                           (4096, True, "ldg")])
 def test_d2d_table_row_follows_shape(n, odd, variant):
     # 16 KiB D2D chunks take the bulk row only for a batch of 256 MiB or more
-    # that is 16-byte aligned; 64 MiB, or 8-byte tails and phases, take LDG.
+    # that is 16-byte aligned; with 8-byte phases that differ, a batch of 128 MiB
+    # or more takes the STAGE row (480 MiB here) and a smaller one LDG (60 MiB).
     w = W.sweep_cell(16, n, "d2d", odd_tails=odd)
     (b,) = w.batches
     p = Pools(w.pools)

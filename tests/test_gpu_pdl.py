@@ -7,9 +7,9 @@ each kernel follows the previous one directly on the stream) must then give
 exactly what the same hops give one after the other on the CPU: each hop reads
 what the previous hop wrote, and later hops overwrite pools that earlier hops
 read. The hops mix the LDG kernel by position and from the work counter, the
-bulk ring, and device-resident descriptor lists (plan + copy kernels), eagerly
-and as a captured CUDA graph replayed twice. The whole pools, guard bands
-included, are compared byte for byte with the oracle.
+bulk ring, the staged kernel, and device-resident descriptor lists (plan +
+copy kernels), eagerly and as a captured CUDA graph replayed twice. The whole
+pools, guard bands included, are compared byte for byte with the oracle.
 """
 
 import numpy as np
@@ -55,12 +55,12 @@ HOPS = [
     ("h0", "p0", "h2d", {"variant": "ldg", "assign": "dynamic", "cta_budget": 8}),
     ("p0", "p1", "d2d", {"variant": "ldg"}),
     ("p1", "p2", "d2d", {"variant": "bulk", "cta_budget": 64}),
-    ("p2", "p3", "d2d", {"variant": "ldg", "threads": 512, "unroll": 4}),
+    ("p2", "p3", "d2d", {"variant": "stage", "cta_budget": 200}),
     ("p3", "p0", "d2d", {"variant": "ldg"}),                    # overwrites what hop 2 read
     ("p0", "h1", "d2h", {"variant": "ldg", "assign": "dynamic", "cta_budget": 4}),
     ("h1", "p1", "h2d", {"variant": "bulk", "cta_budget": 16}),
     ("p1", "h0", "d2h", {"variant": "ldg"}),                    # h0 was the first source
-    ("h0", "p2", "h2d", {"variant": "ldg"}),
+    ("h0", "p2", "h2d", {"variant": "stage", "stages": 2}),
     ("p2", "p3", "d2d", {"variant": "bulk", "cta_budget": 300}),
 ]
 
