@@ -18,9 +18,11 @@
 //     ranges x 256 KiB;
 //   - the copy engines occupy no SM at all, so the tail policy takes DMA
 //     whenever it stays near the link peak (at most 16 ranges of 1 MiB mean);
-//   - otherwise: the LDG kernel reaches the link peak fastest (throughput);
-//     the one-warp bulk CTAs at a budget of 4 cost the colocated decode
-//     stand-in the least p99 while still sustaining a paced KV burst (tail).
+//   - otherwise: the calibrated table's kernel for the batch (throughput:
+//     LDG over the host link, LDG, the bulk ring or STAGE for D2D by size,
+//     alignment and phase); the one-warp bulk CTAs at a budget of 4 cost the
+//     colocated decode stand-in the least p99 while still sustaining a paced
+//     KV burst (tail).
 #include <cuda_runtime.h>
 
 #include "kvx_internal.h"
@@ -83,10 +85,19 @@ kvx_status kvx_auto_path(const uint64_t *src, const uint64_t *dst, const uint64_
         else
             dma = ranges <= kDmaMaxRangesThroughput && mean >= ranges * kDmaMeanPerRange;
     }
-    if (dma)
+    if (dma) {
         *path = KVX_PATH_DMA;
-    else
-        *path = policy == KVX_POLICY_TAIL ? KVX_PATH_KERNEL_BULK : KVX_PATH_KERNEL_LDG;
+    } else if (policy == KVX_POLICY_TAIL) {
+        *path = KVX_PATH_KERNEL_BULK;
+    } else {
+        kvx_launch l{};
+        st = kvx_select_launch(src, dst, sizes, n, dir, nullptr, &l);
+        if (st != KVX_OK)
+            return st;
+        *path = l.variant == KVX_VARIANT_BULK    ? KVX_PATH_KERNEL_BULK
+                : l.variant == KVX_VARIANT_STAGE ? KVX_PATH_KERNEL_STAGE
+                                                 : KVX_PATH_KERNEL_LDG;
+    }
     return KVX_OK;
 }
 
@@ -101,15 +112,14 @@ kvx_status kvx_copy_batch_auto(const uint64_t *src, const uint64_t *dst, const u
         *path_out = path;
     if (path == KVX_PATH_DMA)
         return kvx_copy_batch_memcpy(src, dst, sizes, n, dir, stream, nullptr);
-    kvx_launch l{};
-    if (path == KVX_PATH_KERNEL_BULK) {
+    if (policy == KVX_POLICY_TAIL) {
+        kvx_launch l{};
         l.variant = KVX_VARIANT_BULK;
         l.cta_budget = kTailBudget;
         l.stages = kTailRing;
-    } else {
-        l.variant = KVX_VARIANT_LDG;
+        return kvx_copy_batch_ex(src, dst, sizes, n, dir, &l, stream);
     }
-    return kvx_copy_batch_ex(src, dst, sizes, n, dir, &l, stream);
+    return kvx_copy_batch_ex(src, dst, sizes, n, dir, nullptr, stream);  // the table's launch, as reported
 }
 
 }  // extern "C"

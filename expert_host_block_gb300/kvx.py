@@ -391,8 +391,9 @@ class DeviceList:
 
 KVX_POLICY_THROUGHPUT, KVX_POLICY_TAIL = 0, 1
 POLICIES = {"throughput": KVX_POLICY_THROUGHPUT, "tail": KVX_POLICY_TAIL}
-KVX_PATH_KERNEL_LDG, KVX_PATH_KERNEL_BULK, KVX_PATH_DMA = 1, 2, 3
-PATHS = {KVX_PATH_KERNEL_LDG: "kernel_ldg", KVX_PATH_KERNEL_BULK: "kernel_bulk", KVX_PATH_DMA: "dma"}
+KVX_PATH_KERNEL_LDG, KVX_PATH_KERNEL_BULK, KVX_PATH_DMA, KVX_PATH_KERNEL_STAGE = 1, 2, 3, 4
+PATHS = {KVX_PATH_KERNEL_LDG: "kernel_ldg", KVX_PATH_KERNEL_BULK: "kernel_bulk", KVX_PATH_DMA: "dma",
+         KVX_PATH_KERNEL_STAGE: "kernel_stage"}
 
 
 def _policy(p) -> int:

@@ -135,12 +135,12 @@ typedef struct kvx_chunk {
 typedef struct kvx_launch {
     int variant;         /* kvx_variant */
     int cta_budget;      /* maximum CTAs; the grid is min(cta_budget, work) */
-    int threads;         /* LDG: threads per CTA, one of 128, 256, 512 */
+    int threads;         /* LDG: threads per CTA, one of 128, 256, 512 (STAGE: always 128) */
     int unroll;          /* LDG: 16-byte loads in flight per lane, one of 2, 4, 8 */
     int stages;          /* BULK: shared-memory ring of stages x KVX_CHUNK_BYTES, 2..12; it is cut
                             into stages of the batch's longest chunk (at most 32 stages).
                             STAGE: 4 KiB units each warp keeps in flight, 2, 4 or 8 */
-    int store_policy;    /* LDG: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
+    int store_policy;    /* LDG and STAGE: 0 default, 1 write-through (.wt), 2 streaming (.cs) */
     int assign;          /* LDG: kvx_assign */
 } kvx_launch;
 
@@ -316,11 +316,17 @@ kvx_status kvx_transfer_destroy(kvx_transfer *t);
  * link peak with no SM used): for KVX_POLICY_THROUGHPUT at most 8 ranges whose
  * mean is at least ranges x 256 KiB (where DMA measured faster than the
  * kernel), for KVX_POLICY_TAIL at most 16 ranges averaging at least 1 MiB.
- * Everything else goes to the copy kernel: the LDG variant with the calibrated
- * budget for THROUGHPUT, the bulk variant with 4 one-warp CTAs for TAIL (the
- * lightest footprint beside a colocated decode). */
+ * Everything else goes to the copy kernel: for THROUGHPUT the variant and
+ * launch the calibrated table picks for the batch (kvx_select_launch with no
+ * request: LDG, the bulk ring or STAGE), for TAIL the bulk variant with 4
+ * one-warp CTAs (the lightest footprint beside a colocated decode). */
 typedef enum kvx_policy { KVX_POLICY_THROUGHPUT = 0, KVX_POLICY_TAIL = 1 } kvx_policy;
-typedef enum kvx_path { KVX_PATH_KERNEL_LDG = 1, KVX_PATH_KERNEL_BULK = 2, KVX_PATH_DMA = 3 } kvx_path;
+typedef enum kvx_path {
+    KVX_PATH_KERNEL_LDG = 1,
+    KVX_PATH_KERNEL_BULK = 2,
+    KVX_PATH_DMA = 3,
+    KVX_PATH_KERNEL_STAGE = 4
+} kvx_path;
 
 /* The path kvx_copy_batch_auto would take (host only; validation level 0). */
 kvx_status kvx_auto_path(const uint64_t *src_addrs, const uint64_t *dst_addrs, const uint64_t *sizes,

@@ -366,6 +366,15 @@ def test_auto_path_rules():
     assert kvx.kvx_auto_path(s, d, np.full(17, M), None, "h2d", "tail") == "kernel_bulk"
     # two ranges with a mean below 2 x 256 KiB: kernel
     assert kvx.kvx_auto_path([1 << 30, 1 << 31], [1 << 40, 1 << 41], [256 << 10, 8], None, "h2d") == "kernel_ldg"
+    # throughput takes the calibrated table's kernel: the bulk ring for 256 MiB of aligned 16 KiB D2D chunks,
+    # STAGE for 256 MiB of D2D chunks whose phases differ; the tail policy keeps its 4 bulk CTAs
+    s = (1 << 32) + 32768 * g.permutation(32768)[:16384].astype(np.uint64)
+    d = (1 << 36) + 32768 * np.arange(16384, dtype=np.uint64)
+    z = np.full(16384, 16384, dtype=np.uint64)
+    assert kvx.kvx_auto_path(s, d, z, None, "d2d") == "kernel_bulk"
+    assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "d2d") == "kernel_stage"
+    assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "d2d", "tail") == "kernel_bulk"
+    assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "h2d") == "kernel_ldg"
     with pytest.raises(kvx.KvxError):
         kvx.kvx_auto_path([1 << 30], [1 << 40], [12], None, "h2d")
     with pytest.raises(kvx.KvxError):

@@ -513,9 +513,16 @@ def test_descriptors_helper_parity(level0):
 
 
 @pytest.mark.parametrize("policy", ["throughput", "tail"])
-@pytest.mark.parametrize("shape", ["few_large", "fragmented"])
+@pytest.mark.parametrize("shape", ["few_large", "fragmented", "d2d_odd_large"])
 def test_auto_policy_paths(policy, shape):
-    if shape == "few_large":
+    direction = "h2d"
+    if shape == "d2d_odd_large":  # ~176 MiB of D2D chunks whose phases differ: the table's STAGE kernel
+        w = W.sweep_cell(16, 12000, "d2d", odd_tails=True)
+        p = Pools(w.pools)
+        b = w.batches[0]
+        direction = "d2d"
+        expect = "kernel_stage" if policy == "throughput" else "kernel_bulk"
+    elif shape == "few_large":
         p = _pools_small("host", "device", body=40 * W.MIB)
         b = _batch([0, 12 * W.MIB, 30 * W.MIB], [8 * W.MIB, 20 * W.MIB, 2 * W.MIB], [4 * W.MIB, 3 * W.MIB, W.MIB],
                    "h2d")
@@ -527,7 +534,7 @@ def test_auto_policy_paths(policy, shape):
         expect = "kernel_ldg" if policy == "throughput" else "kernel_bulk"
     try:
         want = p.expected([b])
-        path = kvx.kvx_copy_batch_auto(*p.addrs(b), None, "h2d", policy, None)
+        path = kvx.kvx_copy_batch_auto(*p.addrs(b), None, direction, policy, None)
         assert path == expect
         torch.cuda.synchronize()
         kvx.kvx_stream_check(None)
