@@ -1016,11 +1016,12 @@ kvx_status bits_status(unsigned bits)
     if (bits & kvx::kDevErrTimeout)
         return fail(KVX_ERR_TIMEOUT, "a bounded device wait gave up (status bits 0x%x)", bits);
     if (bits)
-        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s", bits,
+        return fail(KVX_ERR_DEVICE_FAULT, "device status bits 0x%x:%s%s%s%s", bits,
                     (bits & kvx::kDevErrBadRecord) ? " inconsistent chunk record (longer than KVX_CHUNK_BYTES, or "
                                                      "src and dst out of phase in a phase-matched launch);" : "",
                     (bits & kvx::kDevErrCount) ? " device list count above its capacity (clamped);" : "",
-                    (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "");
+                    (bits & kvx::kDevErrBadDesc) ? " device list descriptor failed validation (skipped);" : "",
+                    (bits & kvx::kDevErrBounds) ? " a chunk outside the debug bounds (skipped);" : "");
     return KVX_OK;
 }
 
@@ -1766,6 +1767,29 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
                                                  : cudaMemcpyDeviceToDevice;
     KVX_CUDA_TRY(cudaMemcpyAsync(reinterpret_cast<void *>(dst), reinterpret_cast<const void *>(src),
                                  (size_t)bytes, kind, static_cast<cudaStream_t>(stream)));
+    return KVX_OK;
+}
+
+kvx_status kvx_debug_bounds(const uint64_t *lo, const uint64_t *hi, size_t n)
+{
+    if (n > KVX_DEBUG_BOUNDS_MAX)
+        return fail(KVX_ERR_CAPACITY, "%zu debug bounds; at most KVX_DEBUG_BOUNDS_MAX (%u)", n,
+                    KVX_DEBUG_BOUNDS_MAX);
+    if (n && (!lo || !hi))
+        return fail(KVX_ERR_INVALID_ARG, "null range array");
+    for (size_t i = 0; i < n; ++i)
+        if (lo[i] >= hi[i])
+            return fail(KVX_ERR_INVALID_ARG, "debug bounds range %zu is empty or reversed", i);
+    // the legacy stream's query fails while any stream of the device captures in global mode
+    bool cap = false;
+    kvx_status st = is_capturing(cudaStreamLegacy, &cap);
+    if (st != KVX_OK)
+        return st;
+    if (cap)
+        return fail(KVX_ERR_CAPTURE, "kvx_debug_bounds synchronises the device");
+    cudaError_t e = kvx::set_debug_bounds(lo, hi, (uint32_t)n);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "setting the debug bounds");
     return KVX_OK;
 }
 

@@ -19,8 +19,9 @@ enum : unsigned {
     kDevErrBadRecord = 2u,  // a chunk record longer than KVX_CHUNK_BYTES, or out of phase for its launch
     kDevErrCount = 4u,      // a device-side descriptor count above the list's capacity (clamped)
     kDevErrBadDesc = 8u,    // a device-side descriptor failed validation (skipped)
+    kDevErrBounds = 16u,    // a chunk (device list: a descriptor) outside the debug bounds (skipped)
 };
-constexpr int kErrWords = 4;
+constexpr int kErrWords = 5;
 
 // Result of the device-list plan kernel, read by the device-list copy kernel.
 struct DevListMeta {
@@ -91,6 +92,10 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
 
 // Set the calling thread's kvx_last_error() message and return `status`.
 kvx_status set_error(kvx_status status, const char *message);
+
+// Replace the current device's debug bounds (kvx_debug_bounds) with the n
+// ranges [lo[i], hi[i]); n == 0 turns the check off. Synchronises the device.
+cudaError_t set_debug_bounds(const uint64_t *lo, const uint64_t *hi, uint32_t n);
 
 // Enqueue the bounded-wait self-test kernel.
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned *err, cudaStream_t stream);

@@ -95,6 +95,24 @@ __device__ __forceinline__ void prefetch_l2(uint64_t p, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// ---- debug pool bounds -------------------------------------------------------
+//
+// While ranges are registered (kvx_debug_bounds), every chunk record a copy
+// kernel loads is checked: its source bytes and its destination bytes must each
+// lie inside one registered range, else the chunk is skipped and kDevErrBounds
+// raised. With none registered the check is one read of the constant cache.
+
+__constant__ uint32_t c_bounds_n;
+__constant__ uint64_t c_bounds[2 * KVX_DEBUG_BOUNDS_MAX];  // lo, hi of range i at 2i, 2i + 1
+
+__device__ __forceinline__ bool in_bounds(uint64_t a, uint64_t len)
+{
+    for (uint32_t i = 0; i < c_bounds_n; ++i)
+        if (a >= c_bounds[2 * i] && a + len <= c_bounds[2 * i + 1] && a + len >= a)
+            return true;
+    return false;
+}
+
 // ---- global memory access (inline PTX) ----------------------------------
 
 __device__ __forceinline__ uint4 ld16(const unsigned char *p)
@@ -294,6 +312,10 @@ __device__ __forceinline__ Rec load_rec(const kvx_chunk *__restrict__ tab, uint6
     r.l = b.x;
     if (r.l > KVX_CHUNK_BYTES) {  // never produced by the host planner
         report(err, kDevErrBadRecord);
+        r.l = 0;
+    }
+    if (c_bounds_n && r.l && !(in_bounds(r.s, r.l) && in_bounds(r.d, r.l))) {
+        report(err, kDevErrBounds);
         r.l = 0;
     }
     return r;
@@ -928,6 +950,8 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
                 const uint64_t a = src[i], b = dst[i];
                 if (((a | b | z) & 7u) || !a || !b || a + z < a || b + z < b || z > (1ull << 40)) {
                     atomicOr(&s_bad, 1u);  // skipped: contributes no chunks
+                } else if (c_bounds_n && !(in_bounds(a, z) && in_bounds(b, z))) {
+                    atomicOr(&s_bad, 2u);  // outside the debug bounds: skipped too
                 } else {
                     c = z / KVX_CHUNK_BYTES + (z % KVX_CHUNK_BYTES != 0);
                     atomicMax(&s_max, (uint32_t)(z < KVX_CHUNK_BYTES ? z : KVX_CHUNK_BYTES));
@@ -970,8 +994,10 @@ __global__ void __launch_bounds__(1024) kvx_devlist_plan_kernel(
         meta->n = n;
         meta->max_chunk = s_max;
         meta->next = 0;
-        if (s_bad)
+        if (s_bad & 1u)
             report(err, kDevErrBadDesc);
+        if (s_bad & 2u)
+            report(err, kDevErrBounds);
     }
 }
 
@@ -1284,6 +1310,24 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
     }
 }
 
+
+cudaError_t set_debug_bounds(const uint64_t *lo, const uint64_t *hi, uint32_t n)
+{
+    uint64_t pairs[2 * KVX_DEBUG_BOUNDS_MAX];
+    for (uint32_t i = 0; i < n; ++i) {
+        pairs[2 * i] = lo[i];
+        pairs[2 * i + 1] = hi[i];
+    }
+    // no copy in flight may see a half-written table
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && n)
+        e = cudaMemcpyToSymbol(c_bounds, pairs, sizeof(uint64_t) * 2 * n);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(c_bounds_n, &n, sizeof(n));
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    return e;
+}
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, unsigned *err, cudaStream_t stream)
 {

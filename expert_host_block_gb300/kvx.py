@@ -58,7 +58,7 @@ EXPORTS = (
     "kvx_validate", "kvx_plan_chunks", "kvx_default_launch", "kvx_set_validate_level",
     "kvx_get_validate_level", "kvx_status_string", "kvx_last_error", "kvx_version", "kvx_select_launch",
     "kvx_stream_check", "kvx_host_alloc", "kvx_host_free", "kvx_copy_batch_memcpy",
-    "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout",
+    "kvx_copy_contiguous", "kvx_copy_batch_noalloc", "kvx_selftest_wait_timeout", "kvx_debug_bounds",
     "kvx_devlist_create", "kvx_devlist_destroy", "kvx_copy_device_list",
     "kvx_transfer_create", "kvx_transfer_start", "kvx_transfer_poll", "kvx_transfer_progress",
     "kvx_transfer_destroy", "kvx_auto_path", "kvx_copy_batch_auto", "kvx_device_query",
@@ -128,6 +128,7 @@ def _load():
         "kvx_copy_batch_memcpy": ([_vp, _vp, _vp, _sz, _int, _vp, ctypes.POINTER(_sz)], _int),
         "kvx_copy_contiguous": ([_u64, _u64, _u64, _int, _vp], _int),
         "kvx_selftest_wait_timeout": ([_u64, _vp], _int),
+        "kvx_debug_bounds": ([_vp, _vp, _sz], _int),
         "kvx_copy_batch_noalloc": ([_vp, _vp, _vp, _sz, _int, _int, _vp], _int),
         "kvx_devlist_create": ([ctypes.c_uint32, ctypes.POINTER(_vp)], _int),
         "kvx_transfer_create": ([ctypes.POINTER(_vp)], _int),
@@ -604,6 +605,19 @@ def kvx_copy_batch_noalloc(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, cta
     s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
     _check(_load().kvx_copy_batch_noalloc(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
                                           int(cta_budget), _stream(stream)))
+
+
+KVX_DEBUG_BOUNDS_MAX = 64
+
+
+def kvx_debug_bounds(lo, hi) -> None:
+    """Register the address ranges [lo[i], hi[i]) every copy must stay inside (empty: check off)."""
+    a = np.ascontiguousarray(np.asarray(lo, dtype=np.uint64).reshape(-1))
+    b = np.ascontiguousarray(np.asarray(hi, dtype=np.uint64).reshape(-1))
+    if a.size != b.size:
+        raise ValueError("lo and hi differ in length")
+    _check(_load().kvx_debug_bounds(a.ctypes.data if a.size else None, b.ctypes.data if b.size else None,
+                                    a.size))
 
 
 def kvx_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:

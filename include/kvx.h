@@ -116,7 +116,8 @@ typedef enum kvx_status {
     KVX_ERR_NOT_MAPPED = 5,   /* (validation level 2) an address is not of the kind dir names */
     KVX_ERR_CUDA = 6,         /* a CUDA runtime call failed; see kvx_last_error() */
     KVX_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (reported by kvx_stream_check) */
-    KVX_ERR_DEVICE_FAULT = 8, /* the device reported an inconsistent chunk record */
+    KVX_ERR_DEVICE_FAULT = 8, /* the device reported an inconsistent chunk record, or a chunk outside
+                                 the debug bounds (kvx_debug_bounds) */
     KVX_ERR_CAPTURE = 9       /* the call is not allowed while `stream` is being captured */
 } kvx_status;
 
@@ -506,6 +507,32 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
 kvx_status kvx_copy_batch_noalloc(const uint64_t *src_addrs, const uint64_t *dst_addrs,
                                   const uint64_t *sizes, size_t n, int dir, int cta_budget,
                                   void *stream);
+
+/* ---- debug bounds: a kernel-side check of every chunk ------------------- */
+
+/* Most address ranges kvx_debug_bounds takes per device. */
+#define KVX_DEBUG_BOUNDS_MAX 64u
+
+/* A debugging aid for callers whose descriptors come from code they do not
+ * trust yet (a block manager or router that writes addresses). Register the
+ * memory that copies may touch, typically the host and device pools: n ranges
+ * [lo[i], hi[i]) for the current device, at most KVX_DEBUG_BOUNDS_MAX; n == 0
+ * turns the check off (the initial state). While ranges are registered every
+ * copy kernel checks each chunk it is about to move: its source bytes and its
+ * destination bytes must each lie inside one registered range. A chunk that
+ * does not is skipped (its destination is not written) and the device's
+ * error flags report it, so the next kvx_stream_check / kvx_status_wait on the
+ * device returns KVX_ERR_DEVICE_FAULT; the other chunks are copied. For a
+ * device-resident descriptor list the unit is the whole descriptor. The check
+ * never traps and never reads or writes outside the registered ranges on a
+ * skipped chunk's behalf. It costs one constant-cache read per chunk record
+ * while off, and a scan of the ranges per chunk while on.
+ * This call synchronises the device (no copy may be in flight while the table
+ * changes) and is not allowed during stream capture. KVX_ERR_INVALID_ARG for
+ * null arrays with n > 0, or an empty or reversed range; KVX_ERR_CAPACITY for
+ * n > KVX_DEBUG_BOUNDS_MAX. The pages describe no such check: it guards
+ * against a descriptor that points outside its pools. */
+kvx_status kvx_debug_bounds(const uint64_t *lo, const uint64_t *hi, size_t n);
 
 /* ---- self-test of the bounded device wait ------------------------------- */
 

@@ -564,3 +564,15 @@ def test_nvtx_switch_accepted():
         out = _run_with_env(code, KVX_NVTX=v)
         assert out.returncode == 0, out.stderr
         assert out.stdout.split() == [str(kvx.KVX_VARIANT_LDG), str(kvx.KVX_ERR_ALIGN)]
+
+
+def test_debug_bounds_argument_errors_need_no_device():
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_debug_bounds(np.arange(65, dtype=np.uint64) << np.uint64(20),
+                             (np.arange(65, dtype=np.uint64) + np.uint64(1)) << np.uint64(20))
+    assert e.value.status == kvx.KVX_ERR_CAPACITY
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_debug_bounds([4096, 1 << 20], [8192, 1 << 19])  # the second range is reversed
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        kvx.kvx_debug_bounds([4096], [])
