@@ -206,3 +206,39 @@ def test_device_list_chain_back_to_back():
         for dl in lists:
             dl.close()
         p.close()
+
+
+@pytest.mark.parametrize("variant", ["ldg", "stage", "bulk"])
+def test_foreign_kernels_around_copies(variant):
+    # PyTorch kernels (launched without programmatic serialisation) write a copy's
+    # source right before it and read its destination right after it, on the same
+    # stream with no synchronisation: each must still see the other's bytes.
+    n, size = 2048, 16384
+    src = torch.zeros(n * size // 4, dtype=torch.int32, device="cuda")
+    mid = torch.zeros_like(src)
+    out = torch.zeros_like(src)
+    g = np.random.default_rng([W.SEED, 97])
+    perm = g.permutation(n).astype(np.uint64)
+    z = np.full(n, size, dtype=np.uint64)
+    off = np.arange(n, dtype=np.uint64) * np.uint64(size)
+    a = kvx.DescBuf(n)  # src -> mid, blocks permuted
+    b = kvx.DescBuf(n)  # mid -> out, back in order
+    a.upload(np.uint64(src.data_ptr()) + off, np.uint64(mid.data_ptr()) + perm * np.uint64(size), z, "d2d")
+    b.upload(np.uint64(mid.data_ptr()) + perm * np.uint64(size), np.uint64(out.data_ptr()) + off, z, "d2d")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    launch = {"variant": variant}
+    try:
+        with torch.cuda.stream(s):
+            for step in range(1, 6):
+                src.fill_(step)                  # torch writes the source
+                a.copy(stream=s, launch=launch)  # kvx copies it
+                mid.add_(10)                     # torch rewrites the copy's output in place
+                b.copy(stream=s, launch=launch)
+                out.mul_(2)                      # torch reads and writes the second copy's output
+        kvx.kvx_stream_check(s)
+        assert torch.all(out == 2 * (5 + 10)).item()
+        assert torch.all(mid == 5 + 10).item()
+    finally:
+        a.close()
+        b.close()
