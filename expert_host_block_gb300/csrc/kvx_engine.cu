@@ -83,6 +83,7 @@ struct TableRow {
     kvx_launch cfg;
     uint64_t min_payload = 0;  // ... and the batch carries at least this many bytes
     bool unmatched_only = false;  // ... and (when set) some chunk's src and dst differ mod 16
+    uint64_t max_payload = ~0ull; // ... and at most this many bytes
 };
 
 struct EnvSettings {
@@ -98,12 +99,13 @@ struct EnvSettings {
 
 // A launch table in a text file: one row per line, `#` starts a comment:
 //   dir max_mean_chunk_bytes variant cta_budget threads unroll stages store_policy
-//       [assign [min_payload_bytes [phase]]]
+//       [assign [min_payload_bytes [phase [max_payload_bytes]]]]
 // with dir h2d|d2h|d2d, max_mean_chunk_bytes an integer or "inf", variant
 // ldg|bulk|stage, assign static|dynamic|auto (absent or auto: the built-in
 // choice for dir), min_payload_bytes an integer (absent: 0), phase any|unmatched
 // (unmatched: only batches with a chunk whose src and dst differ mod 16; absent:
-// any). Rows are tried in file order, before the built-in rows.
+// any), max_payload_bytes an integer or "inf" (absent: inf). Rows are tried in
+// file order, before the built-in rows.
 std::string parse_table(const char *path, std::vector<TableRow> *rows)
 {
     FILE *f = fopen(path, "r");
@@ -116,10 +118,10 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         ++lineno;
         if (char *h = strchr(line, '#'))
             *h = 0;
-        char dir[16], maxs[32], var[16], asg[16] = "", minp[32] = "", phase[16] = "";
+        char dir[16], maxs[32], var[16], asg[16] = "", minp[32] = "", phase[16] = "", maxp[32] = "";
         int budget, threads, unroll, stages, policy;
-        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s %31s %15s", dir, maxs, var, &budget,
-                               &threads, &unroll, &stages, &policy, asg, minp, phase);
+        const int got = sscanf(line, "%15s %31s %15s %d %d %d %d %d %15s %31s %15s %31s", dir, maxs, var, &budget,
+                               &threads, &unroll, &stages, &policy, asg, minp, phase, maxp);
         if (got <= 0)
             continue;  // blank or comment
         TableRow r{};
@@ -135,6 +137,9 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
                                                     : -1;
         const int ph = (got < 11 || !strcmp(phase, "any")) ? 0 : !strcmp(phase, "unmatched") ? 1 : -1;
         r.unmatched_only = ph == 1;
+        char *xend = nullptr;
+        if (got >= 12 && strcmp(maxp, "inf"))
+            r.max_payload = strtoull(maxp, &xend, 10);
         const int assign = (got < 9 || !strcmp(asg, "auto")) ? KVX_ASSIGN_AUTO
                            : !strcmp(asg, "static") ? KVX_ASSIGN_STATIC
                            : !strcmp(asg, "dynamic") ? KVX_ASSIGN_DYNAMIC : -1;
@@ -144,11 +149,12 @@ std::string parse_table(const char *path, std::vector<TableRow> *rows)
         if (got < 8 || r.dir < 0 || variant < 0 || (end && *end) || budget < 1 ||
             (threads != 128 && threads != 256 && threads != 512) || (unroll != 2 && unroll != 4 && unroll != 8) ||
             stages < 2 || stages > 12 || policy < 0 || policy > 2 || assign < 0 || (pend && *pend) ||
-            (got >= 10 && !isdigit((unsigned char)minp[0])) || ph < 0 ||
+            (got >= 10 && !isdigit((unsigned char)minp[0])) || ph < 0 || (xend && *xend) ||
+            (got >= 12 && strcmp(maxp, "inf") && !isdigit((unsigned char)maxp[0])) ||
             (variant == KVX_VARIANT_STAGE && stages != 2 && stages != 4 && stages != 8)) {
             err = std::string("KVX_TABLE=") + path + ": line " + std::to_string(lineno) +
                   " is not 'dir max_mean_chunk variant cta_budget threads unroll stages store_policy "
-                  "[assign [min_payload [phase]]]'";
+                  "[assign [min_payload [phase [max_payload]]]]'";
             break;
         }
         r.cfg = kvx_launch{variant, budget, threads, unroll, stages, policy, assign};
@@ -582,10 +588,18 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 65,536 0.936 against 0.898, 16 KiB x 32,768 0.948 against 0.921, 28 KiB x
 // 18,724 0.942 against 0.920. Smaller ones stay with LDG (16 KiB x 4,096 odd:
 // 0.890 LDG against 0.856), as do matched batches (phase-matched LDG: 0.97-0.99).
+//
+// D2D batches of at most 24 MiB take one 512-thread CTA per SM: timed alone a
+// 16 MiB batch is launch-bound with any grid (0.49 of HBM), but as a stream
+// of batches (programmatic dependent launch) 152 CTAs hand over to the next
+// batch faster than 1,216: 4 KiB x 4,096 back to back 0.845 of HBM, 0.83 with
+// 304 x 256, 0.73-0.77 with 1,216 x 128. From 32 MiB up the 1,216-CTA row is
+// as fast or faster (8 KiB x 4,096: 0.895-0.909 against 0.885).
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 1216, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
     {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
@@ -604,6 +618,7 @@ struct BatchShape {
 bool row_matches(const TableRow &r, int dir, const BatchShape &b)
 {
     return r.dir == dir && b.mean_chunk <= r.max_mean_chunk && b.payload >= r.min_payload &&
+           b.payload <= r.max_payload &&
            (b.aligned || r.cfg.variant != KVX_VARIANT_BULK) && (!r.unmatched_only || !b.matched);
 }
 

@@ -393,7 +393,8 @@ def test_kvx_table_file_overrides_rows(tmp_path):
                      "h2d inf ldg 33 512 4 3 1 static\n"
                      "d2d inf bulk 11 256 8 4 0 auto 1099511627776\n"  # batches of 1 TiB and more
                      "d2d inf ldg 99 512 8 3 0 dynamic\n"
-                     "d2h inf stage 21 128 8 2 0 auto 0 unmatched\n")
+                     "d2h inf stage 21 128 8 2 0 auto 0 unmatched\n"
+                     "d2h inf ldg 13 512 8 3 0 auto 0 any 65536\n")
     code = ("from expert_host_block_gb300 import kvx\n"
             "print(kvx.kvx_default_launch('h2d', 4096))\n"
             "print(kvx.kvx_default_launch('h2d', 16384))\n"
@@ -418,12 +419,24 @@ def test_kvx_table_file_overrides_rows(tmp_path):
              "print(kvx.kvx_select_launch(s + np.uint64(8), d, z, None, 'd2h')['variant'])\n")
     out = _run_with_env(code2, KVX_TABLE=str(table))
     assert out.stdout.split() == ["1", "3"], out.stdout + out.stderr
+    # the max_payload column: a d2h batch of at most 64 KiB takes the 512-thread row (after the stage
+    # row, which it matches only with phases that differ); a bigger one the built-in 256-thread row
+    code3 = ("import numpy as np\n"
+             "from expert_host_block_gb300 import kvx\n"
+             "i = np.arange(16, dtype=np.uint64)\n"
+             "s = np.uint64(1 << 36) + i * np.uint64(8192)\n"
+             "d = np.uint64(1 << 32) + i * np.uint64(8192)\n"
+             "print(kvx.kvx_select_launch(s, d, np.full(16, 4096, dtype=np.uint64), None, 'd2h')['threads'])\n"
+             "print(kvx.kvx_select_launch(s, d, np.full(16, 8192, dtype=np.uint64), None, 'd2h')['threads'])\n")
+    out = _run_with_env(code3, KVX_TABLE=str(table))
+    assert out.stdout.split() == ["512", "256"], out.stdout + out.stderr
 
 
 @pytest.mark.parametrize("text", ["h2d 4096 tma 8 256 8 3 0\n", "h2d 4096 ldg 8 300 8 3 0\n",
                                   "x2y inf ldg 8 256 8 3 0\n", "h2d inf ldg 8 256 8\n",
                                   "h2d inf ldg 8 256 8 3 0 greedy\n", "h2d inf ldg 8 256 8 3 0 auto 12x\n",
-                                  "d2d inf stage 8 128 8 3 0\n", "d2d inf ldg 8 256 8 3 0 auto 0 odd\n"])
+                                  "d2d inf stage 8 128 8 3 0\n", "d2d inf ldg 8 256 8 3 0 auto 0 odd\n",
+                                  "d2d inf ldg 8 256 8 3 0 auto 0 any 12q\n"])
 def test_kvx_table_malformed_is_an_error(tmp_path, text):
     table = tmp_path / "bad.table"
     table.write_text(text)
@@ -526,6 +539,18 @@ def test_select_launch_stage_row_for_mismatched_phases():
     with pytest.raises(kvx.KvxError) as e:
         kvx.kvx_select_launch(*_batch(100, 16384), None, "h2d", {"variant": "stage", "stages": 3})
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+
+
+def test_select_launch_small_d2d_row():
+    # D2D batches of at most 24 MiB: one 512-thread CTA per SM; from just above it, the 1,216-CTA row
+    small = kvx.kvx_select_launch(*_batch(6144, 4096), None, "d2d")  # 24 MiB
+    assert (small["variant"], small["threads"], small["unroll"]) == (kvx.KVX_VARIANT_LDG, 512, 8)
+    assert small["cta_budget"] == 152  # 6,144 units need 384 CTAs of 16 warps: the budget binds
+    assert kvx.kvx_select_launch(*_batch(1024, 4096), None, "d2d")["cta_budget"] == 64  # 1,024 units: the work binds
+    big = kvx.kvx_select_launch(*_batch(6146, 4096), None, "d2d")
+    assert (big["threads"], big["cta_budget"]) == (128, 1216)
+    # host-link batches of any size keep their row
+    assert kvx.kvx_select_launch(*_batch(4096, 4096), None, "h2d")["threads"] == 256
 
 
 def test_select_launch_rejects_what_copy_batch_rejects():
