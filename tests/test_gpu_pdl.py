@@ -242,3 +242,22 @@ def test_foreign_kernels_around_copies(variant):
     finally:
         a.close()
         b.close()
+
+
+def test_chain_with_programmatic_launch_off():
+    # KVX_PDL=0: the same kernels launched without the attribute (plain stream order); a chain of
+    # uploaded copies and the smoke batch still match the oracle
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys\n"
+            "sys.path.insert(0, 'tests')\n"
+            "import __graft_entry__ as g\n"
+            "g.smoke()\n"
+            "import test_gpu_pdl as t\n"  # smoke() has built the library and selected cuda:0
+            "t.test_uploaded_chain_back_to_back(1)\n"
+            "print('chain ok')\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=root,
+                         env=dict(os.environ, KVX_PDL="0"))
+    assert out.returncode == 0 and "smoke ok" in out.stdout and "chain ok" in out.stdout, out.stdout + out.stderr
