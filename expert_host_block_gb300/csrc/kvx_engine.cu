@@ -31,6 +31,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "kvx_internal.h"
@@ -1090,6 +1091,34 @@ kvx_status kvx::set_error(kvx_status status, const char *message)
     return fail(status, "%s", message);
 }
 
+namespace {
+std::mutex g_handles_mu;
+std::unordered_map<const void *, int> g_handles;  // live handle -> its kvx::HandleKind
+}  // namespace
+
+void kvx::handle_add(const void *h, HandleKind kind)
+{
+    std::lock_guard<std::mutex> g(g_handles_mu);
+    g_handles[h] = kind;
+}
+
+bool kvx::handle_remove(const void *h, HandleKind kind)
+{
+    std::lock_guard<std::mutex> g(g_handles_mu);
+    auto it = g_handles.find(h);
+    if (it == g_handles.end() || it->second != kind)
+        return false;
+    g_handles.erase(it);
+    return true;
+}
+
+bool kvx::handle_live(const void *h, HandleKind kind)
+{
+    std::lock_guard<std::mutex> g(g_handles_mu);
+    auto it = g_handles.find(h);
+    return it != g_handles.end() && it->second == kind;
+}
+
 // ---------------------------------------------------------------------------
 // descriptor buffers
 // ---------------------------------------------------------------------------
@@ -1326,6 +1355,7 @@ kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
         return cuda_fail(e, "kvx_desc_buf_create");
     }
     b->cap = max_chunks;
+    kvx::handle_add(b, kvx::kHandleDescBuf);
     *out = b;
     return KVX_OK;
 }
@@ -1337,6 +1367,8 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *b, const uint64_t *src, const ui
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!b)
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    if (!kvx::handle_live(b, kvx::kHandleDescBuf))
+        return fail(KVX_ERR_INVALID_ARG, "not a live descriptor buffer (destroyed, or never created)");
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
@@ -1387,6 +1419,8 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!b)
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    if (!kvx::handle_live(b, kvx::kHandleDescBuf))
+        return fail(KVX_ERR_INVALID_ARG, "not a live descriptor buffer (destroyed, or never created)");
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
@@ -1463,6 +1497,8 @@ kvx_status kvx_desc_buf_info(const kvx_desc_buf *b, size_t *n_chunks, uint64_t *
 {
     if (!b)
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
+    if (!kvx::handle_live(b, kvx::kHandleDescBuf))
+        return fail(KVX_ERR_INVALID_ARG, "not a live descriptor buffer (destroyed, or never created)");
     if (n_chunks)
         *n_chunks = b->n_chunks;
     if (payload)
@@ -1476,6 +1512,8 @@ kvx_status kvx_desc_buf_destroy(kvx_desc_buf *b)
 {
     if (!b)
         return KVX_OK;
+    if (!kvx::handle_remove(b, kvx::kHandleDescBuf))
+        return fail(KVX_ERR_INVALID_ARG, "not a live descriptor buffer (destroyed, or never created)");
     if (b->upload_recorded)
         cudaEventSynchronize(b->upload_done);
     if (b->use_recorded)
@@ -1523,6 +1561,7 @@ kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out)
         return cuda_fail(e, "kvx_devlist_create");
     }
     l->offsets = reinterpret_cast<uint64_t *>(reinterpret_cast<char *>(l->meta) + 256);
+    kvx::handle_add(l, kvx::kHandleDevList);
     *out = l;
     return KVX_OK;
 }
@@ -1531,6 +1570,8 @@ kvx_status kvx_devlist_destroy(kvx_devlist *l)
 {
     if (!l)
         return KVX_OK;
+    if (!kvx::handle_remove(l, kvx::kHandleDevList))
+        return fail(KVX_ERR_INVALID_ARG, "not a live device list (destroyed, or never created)");
     if (l->use_recorded)
         cudaEventSynchronize(l->last_use);
     cudaFree(l->meta);
@@ -1546,6 +1587,8 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (!l)
         return fail(KVX_ERR_INVALID_ARG, "null device list");
+    if (!kvx::handle_live(l, kvx::kHandleDevList))
+        return fail(KVX_ERR_INVALID_ARG, "not a live device list (destroyed, or never created)");
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;

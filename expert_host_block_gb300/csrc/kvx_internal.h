@@ -93,6 +93,16 @@ cudaError_t launch_devlist(const Launch &l, const uint64_t *src, const uint64_t 
 // Set the calling thread's kvx_last_error() message and return `status`.
 kvx_status set_error(kvx_status status, const char *message);
 
+// The live handles of the library's opaque objects. Every entry point that
+// takes a handle looks it up before touching it, so a destroyed handle, or a
+// pointer that never was one, is KVX_ERR_INVALID_ARG instead of a use after
+// free. (Destroying a handle while another thread still uses it remains the
+// caller's error.)
+enum HandleKind : int { kHandleDescBuf = 1, kHandleDevList = 2, kHandleTransfer = 3 };
+void handle_add(const void *h, HandleKind kind);
+bool handle_remove(const void *h, HandleKind kind);  // false: not a live handle of that kind
+bool handle_live(const void *h, HandleKind kind);
+
 // Replace the current device's debug bounds (kvx_debug_bounds) with the n
 // ranges [lo[i], hi[i]); n == 0 turns the check off. Synchronises the device.
 cudaError_t set_debug_bounds(const uint64_t *lo, const uint64_t *hi, uint32_t n);

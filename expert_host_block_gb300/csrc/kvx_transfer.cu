@@ -59,6 +59,7 @@ kvx_status kvx_transfer_create(kvx_transfer **out)
     kvx_transfer *t = new (std::nothrow) kvx_transfer;
     if (!t)
         return KVX_ERR_CAPACITY;
+    kvx::handle_add(t, kvx::kHandleTransfer);
     *out = t;
     return KVX_OK;
 }
@@ -69,6 +70,8 @@ kvx_status kvx_transfer_start(kvx_transfer *t, const uint64_t *src, const uint64
 {
     if (!t)
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_start: null transfer");
+    if (!kvx::handle_live(t, kvx::kHandleTransfer))
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_start: not a live transfer");
     if (t->in_flight)
         return kvx::set_error(KVX_ERR_INVALID_ARG,
                               "kvx_transfer_start: a piece of the previous transfer is still in flight");
@@ -100,6 +103,8 @@ kvx_status kvx_transfer_poll(kvx_transfer *t, int *done)
 {
     if (!t || !done)
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_poll: null argument");
+    if (!kvx::handle_live(t, kvx::kHandleTransfer))
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_poll: not a live transfer");
     *done = 0;
     if (t->in_flight) {
         const cudaError_t e = cudaEventQuery(t->done_ev);
@@ -120,7 +125,9 @@ kvx_status kvx_transfer_poll(kvx_transfer *t, int *done)
 kvx_status kvx_transfer_progress(const kvx_transfer *t, size_t *submitted, size_t *total)
 {
     if (!t)
-        return KVX_ERR_INVALID_ARG;
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_progress: null transfer");
+    if (!kvx::handle_live(t, kvx::kHandleTransfer))
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_progress: not a live transfer");
     if (submitted)
         *submitted = t->next;
     if (total)
@@ -132,6 +139,8 @@ kvx_status kvx_transfer_destroy(kvx_transfer *t)
 {
     if (!t)
         return KVX_OK;
+    if (!kvx::handle_remove(t, kvx::kHandleTransfer))
+        return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_destroy: not a live transfer");
     if (t->in_flight)
         cudaEventSynchronize(t->done_ev);
     if (t->done_ev)

@@ -60,6 +60,11 @@
  *     kvx_last_error() gives a one-line message for the calling thread.
  *     Device-side errors (a bounded wait that gave up) are reported by
  *     kvx_stream_check. No entry point aborts the process or traps the GPU.
+ *   - Opaque handles (kvx_desc_buf, kvx_devlist, kvx_transfer): kvx keeps a
+ *     registry of the live ones, so passing a destroyed handle, or a pointer
+ *     that never was one, returns KVX_ERR_INVALID_ARG without touching it
+ *     (destroying a handle twice included). Destroying a handle while another
+ *     thread is inside a call with it is the caller's error.
  */
 #ifndef KVX_H
 #define KVX_H

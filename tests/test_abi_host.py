@@ -6,11 +6,13 @@ validation level, status strings) and error paths that return before any
 CUDA call.
 """
 
+import ctypes
 import glob
 import os
 import re
 import subprocess
 import sys
+import types
 
 import numpy as np
 import pytest
@@ -601,3 +603,39 @@ def test_debug_bounds_argument_errors_need_no_device():
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         kvx.kvx_debug_bounds([4096], [])
+
+
+def test_stale_and_bogus_handles_are_argument_errors():
+    # A destroyed handle, a pointer that never was a handle, or a handle of another
+    # kind is rejected before the library touches it (no device needed).
+    lib = kvx._load()
+    t = kvx.Transfer()
+    stale = t.handle
+    t.close()
+    done = ctypes.c_int()
+    assert lib.kvx_transfer_poll(stale, ctypes.byref(done)) == kvx.KVX_ERR_INVALID_ARG
+    assert lib.kvx_transfer_progress(stale, None, None) == kvx.KVX_ERR_INVALID_ARG
+    assert lib.kvx_transfer_destroy(stale) == kvx.KVX_ERR_INVALID_ARG  # destroyed twice
+    assert "not a live transfer" in kvx.last_error()
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.Transfer.start(types.SimpleNamespace(handle=stale), [8], [16], [8], "h2d")
+    assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+
+    bogus = ctypes.create_string_buffer(4096)
+    addr = ctypes.addressof(bogus)
+    live = kvx.Transfer()  # a live handle of the wrong kind
+    try:
+        for h in (addr, live.handle):
+            for call in (lambda: kvx.kvx_desc_buf_info(h),
+                         lambda: kvx.kvx_copy_uploaded(h),
+                         lambda: kvx.kvx_upload_descriptors(h, [8], [16], [8], None, "h2d"),
+                         lambda: kvx.kvx_desc_buf_destroy(h),
+                         lambda: kvx.kvx_devlist_destroy(h),
+                         lambda: kvx.kvx_copy_device_list(h, 8, 8, 8, 4, "d2d")):
+                with pytest.raises(kvx.KvxError) as e:
+                    call()
+                assert e.value.status == kvx.KVX_ERR_INVALID_ARG and "not a live" in str(e.value)
+        assert bytes(bogus.raw) == bytes(4096)  # never written
+        assert live.progress() == (0, 0)  # the live transfer is untouched
+    finally:
+        live.close()
