@@ -99,3 +99,20 @@ def test_parse_cell_specs():
     for bad in ("x2y:4:16", "h2d:4", "h2d:4:16:even", "d2h:4:16:odd:1"):
         with pytest.raises(SystemExit):
             bench.parse_cell(bad)
+
+
+def test_graded_passes_rotate_and_take_medians():
+    specs = bench.graded_specs()
+    seen_first = set()
+    for r in range(bench.GRADED_ROUNDS):
+        order = bench.rotated(specs, r, bench.GRADED_ROUNDS)
+        assert sorted(order) == sorted(specs)  # every cell once per pass
+        seen_first.add(order[0])
+    assert len(seen_first) == bench.GRADED_ROUNDS  # each pass starts elsewhere
+    base = {"dir": "h2d", "size_kib": 4, "n": 4096, "odd": False, "kernel_gbs_best": 0.0}
+    rounds = [dict(base, **{k: v for k in bench.ROUND_FIELDS}, kernel_gbs_best=v) for v in (0.9, 0.5, 0.8)]
+    rounds[1]["frac_stream"] = None  # a figure missing from one pass
+    c = bench.median_of_rounds(rounds)
+    assert c["frac"] == c["kernel_gbs"] == 0.8  # one disturbed pass does not move the cell
+    assert c["frac_stream"] == pytest.approx(0.85)  # median of the passes that have it
+    assert c["kernel_gbs_best"] == 0.9 and c["rounds"] == 3 and c["dir"] == "h2d"
