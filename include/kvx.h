@@ -413,7 +413,7 @@ kvx_status kvx_stream_check(void *stream);
 /* The current device's SM count, per-thread stack limit and free / total
  * memory (any pointer may be NULL): the inputs of a per-device launch profile,
  * and the check against the sm_120 bulk-copy pitfall, where the
- * .shared::cluster destination form made the driver raise the per-thread
+ * cluster-scope destination form made the driver raise the per-thread
  * stack limit and hold 1.37 GiB of device memory (FreeToken issue #751,
  * §What we changed). kvx uses the .shared::cta form, which leaves both
  * unchanged. */

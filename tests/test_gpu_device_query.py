@@ -1,6 +1,6 @@
 """The bulk copy path leaves the per-thread stack limit and device memory alone.
 
-On sm_120 the .shared::cluster form of the bulk copy made the driver raise
+On sm_120 the cluster-scope destination form of the bulk copy made the driver raise
 the per-thread stack limit on first launch and hold 1.37 GiB of device memory
 (FreeToken issue #751, §What we changed). kvx issues the .shared::cta form;
 this checks, in a fresh process, that the first bulk launch changes neither.
