@@ -1424,6 +1424,10 @@ kvx_status kvx_copy_uploaded_ex(kvx_desc_buf *b, const kvx_launch *want, void *s
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
+    // One call at a time per buffer: the wait on the previous copy, the launch
+    // and the record of this one go together, so copies from several threads
+    // never overlap on the buffer's table (and its work counter).
+    std::lock_guard<std::mutex> g(b->mu);
     kvx_launch merged = b->selected;
     if (want) {
         if (want->variant < 0 || want->variant > KVX_VARIANT_STAGE || want->cta_budget < 0)

@@ -222,7 +222,8 @@ kvx_status kvx_upload_descriptors(kvx_desc_buf *buf, const uint64_t *src_addrs,
  * dynamic-assignment copy keeps its work counter in the buffer): outside
  * capture, each copy first makes `stream` wait for the buffer's previous copy
  * (free when that was on the same stream); graph replays are the caller's to
- * order. */
+ * order. Calls on one buffer from several threads are serialised by the
+ * buffer (uploads and copies alike), so their copies never overlap. */
 kvx_status kvx_copy_uploaded(kvx_desc_buf *buf, int cta_budget, void *stream);
 
 /* kvx_copy_uploaded with an explicit launch configuration (NULL = table): the

@@ -70,3 +70,48 @@ def test_concurrent_callers(threads):
         p.assert_equal(want)
     finally:
         p.close()
+
+
+def test_threads_share_one_descriptor_buffer():
+    # Four threads copy the same uploaded H2D buffer (units taken from the table's
+    # counter) on their own streams. The buffer serialises their calls and orders
+    # each copy after the previous one, so no two copies share the counter: after
+    # all of them, one more copy into a fresh canary pool must still be exact.
+    w = W.kv_burst(n_sets=1, n_per_dir=8192, pool_bytes=W.GIB // 4)
+    p = Pools(w.pools)
+    try:
+        h2d = w.batches[0][0]
+        want = p.expected([h2d])
+        buf = kvx.DescBuf(h2d.n)
+        buf.upload(*p.addrs(h2d), "h2d")
+        torch.cuda.synchronize()
+        launch = {"variant": "ldg", "assign": "dynamic", "cta_budget": 16}
+        errors = []
+
+        def worker():
+            try:
+                torch.cuda.set_device(0)
+                s = torch.cuda.Stream()
+                for _ in range(25):
+                    buf.copy(stream=s, launch=launch)
+                kvx.kvx_stream_check(s)
+            except Exception as e:  # surfaced below
+                errors.append(repr(e))
+
+        ts = [threading.Thread(target=worker) for _ in range(4)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        assert not errors, errors
+        torch.cuda.synchronize()
+        p.assert_equal(want)
+        p.bufs["dev"].fill_(W.CANARY)
+        torch.cuda.synchronize()
+        want = p.expected([h2d])
+        buf.copy(launch=launch)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+        buf.close()
+    finally:
+        p.close()
