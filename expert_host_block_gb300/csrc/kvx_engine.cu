@@ -1150,6 +1150,8 @@ struct kvx_devlist {
     uint64_t *offsets = nullptr;
     cudaEvent_t last_use = nullptr;
     bool use_recorded = false;
+    unsigned long long last_stream = 0;  // cudaStreamGetId of the stream of the last copy
+    std::mutex mu;
 };
 
 // ---------------------------------------------------------------------------
@@ -1632,12 +1634,23 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
     st = is_capturing(stream, &cap);
     if (st != KVX_OK)
         return st;
+    // The list's scratch serves one copy at a time: outside capture, order this
+    // copy after the list's previous one when that ran on another stream (same
+    // stream: ordered already, and a wait would cancel the launch overlap).
+    std::lock_guard<std::mutex> g(l->mu);
+    unsigned long long sid = 0;
+    if (!cap) {
+        KVX_CUDA_TRY(cudaStreamGetId(stream, &sid));
+        if (l->use_recorded && l->last_stream != sid)
+            KVX_CUDA_TRY(cudaStreamWaitEvent(stream, l->last_use, 0));
+    }
     cudaError_t e = kvx::launch_devlist(lc, src, dst, sizes, count, l->max_n, l->meta, l->offsets, l->err, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "device-list launch");
     if (!cap) {
         KVX_CUDA_TRY(cudaEventRecord(l->last_use, stream));
         l->use_recorded = true;
+        l->last_stream = sid;
     }
     return KVX_OK;
 }

@@ -1028,7 +1028,10 @@ __device__ __forceinline__ Rec devlist_rec(uint64_t u, uint64_t total, uint32_t 
     Rec r;
     r.s = src[lo] + off;
     r.d = dst[lo] + off;
-    r.l = (uint32_t)(z - off < KVX_CHUNK_BYTES ? z - off : KVX_CHUNK_BYTES);
+    // off < z always holds for a scan of these arrays; a scan left by another
+    // list's copy (scratch used by two copies at once) copies nothing here
+    // instead of running past the descriptor
+    r.l = off < z ? (uint32_t)(z - off < KVX_CHUNK_BYTES ? z - off : KVX_CHUNK_BYTES) : 0u;
     if (pass * unit >= r.l)
         r.l = 0;
     *pass_out = (uint32_t)pass;

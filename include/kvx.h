@@ -274,8 +274,11 @@ kvx_status kvx_devlist_destroy(kvx_devlist *list);                /* waits for i
  * kvx_stream_check as KVX_ERR_DEVICE_FAULT: a count above max_n (only max_n
  * descriptors are copied) or a descriptor that fails validation (it is
  * skipped; the others are copied). Overlapping destinations are not
- * detected. The list's scratch is reused by every call: calls with the same
- * list on different streams must not overlap. */
+ * detected. The list's scratch is reused by every call, one copy at a time:
+ * outside capture each call makes `stream` wait for the list's previous copy
+ * when that was on another stream (calls from several threads are serialised
+ * by the list); inside capture, copies of one list on different streams of the
+ * graph are the caller's to order. */
 kvx_status kvx_copy_device_list(kvx_devlist *list, const uint64_t *d_src, const uint64_t *d_dst,
                                 const uint64_t *d_sizes, const uint32_t *d_count, int dir,
                                 const kvx_launch *launch, void *stream);

@@ -201,3 +201,39 @@ def test_empty_list_and_host_errors():
     finally:
         lst.close()
         p.close()
+
+
+def test_one_list_copied_from_two_streams():
+    # Calls of one list alternate between two streams, each with its own arrays and
+    # count: the list's scratch (plan results, chunk offsets) serves one copy at a
+    # time, so each call waits for the list's previous copy on the other stream.
+    specs = {"src": W.PoolSpec("src", "device", 64 * W.MIB, "random", (99,)),
+             "dst": W.PoolSpec("dst", "device", 64 * W.MIB, "canary")}
+    p = Pools(specs)
+    lst = kvx.DeviceList(4096)
+    g = np.random.default_rng([W.SEED, 99])
+    slots = g.permutation(4096)  # 16 KiB slots of the destination, split over the calls
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    arrays, batches, used = [], [], 0
+    try:
+        for k in range(6):
+            n = int(g.integers(200, 600))
+            so = (g.permutation(4096)[:n] * 16384 + 8 * g.integers(0, 2, n)).astype(np.uint64)
+            do = (slots[used:used + n] * 16384 + 8 * g.integers(0, 2, n)).astype(np.uint64)
+            used += n
+            sz = (8 * g.integers(1, 2047, n)).astype(np.uint64)
+            batches.append(W.Batch("src", "dst", so, do, sz, "d2d"))
+        want = p.expected(batches)
+        for k, b in enumerate(batches):
+            a = DevArrays(b.n)
+            a.fill(*p.addrs(b))
+            arrays.append(a)
+        torch.cuda.synchronize()
+        for k, a in enumerate(arrays):
+            lst.copy(*a.ptrs(), "d2d", stream=streams[k % 2])
+        for s in streams:
+            kvx.kvx_stream_check(s)
+        p.assert_equal(want)
+    finally:
+        lst.close()
+        p.close()
