@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -28,6 +29,7 @@ struct kvx_transfer {
     cudaEvent_t done_ev = nullptr;
     bool in_flight = false;
     int device = 0;
+    mutable std::mutex mu;  // start, poll and progress from several threads take turns
 };
 
 namespace {
@@ -58,7 +60,7 @@ kvx_status kvx_transfer_create(kvx_transfer **out)
     *out = nullptr;
     kvx_transfer *t = new (std::nothrow) kvx_transfer;
     if (!t)
-        return KVX_ERR_CAPACITY;
+        return kvx::set_error(KVX_ERR_CAPACITY, "kvx_transfer_create: out of host memory");
     kvx::handle_add(t, kvx::kHandleTransfer);
     *out = t;
     return KVX_OK;
@@ -72,6 +74,7 @@ kvx_status kvx_transfer_start(kvx_transfer *t, const uint64_t *src, const uint64
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_start: null transfer");
     if (!kvx::handle_live(t, kvx::kHandleTransfer))
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_start: not a live transfer");
+    std::lock_guard<std::mutex> g(t->mu);
     if (t->in_flight)
         return kvx::set_error(KVX_ERR_INVALID_ARG,
                               "kvx_transfer_start: a piece of the previous transfer is still in flight");
@@ -105,6 +108,7 @@ kvx_status kvx_transfer_poll(kvx_transfer *t, int *done)
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_poll: null argument");
     if (!kvx::handle_live(t, kvx::kHandleTransfer))
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_poll: not a live transfer");
+    std::lock_guard<std::mutex> g(t->mu);
     *done = 0;
     if (t->in_flight) {
         const cudaError_t e = cudaEventQuery(t->done_ev);
@@ -128,6 +132,7 @@ kvx_status kvx_transfer_progress(const kvx_transfer *t, size_t *submitted, size_
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_progress: null transfer");
     if (!kvx::handle_live(t, kvx::kHandleTransfer))
         return kvx::set_error(KVX_ERR_INVALID_ARG, "kvx_transfer_progress: not a live transfer");
+    std::lock_guard<std::mutex> g(t->mu);
     if (submitted)
         *submitted = t->next;
     if (total)

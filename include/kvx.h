@@ -308,7 +308,8 @@ kvx_status kvx_transfer_start(kvx_transfer *t, const uint64_t *src_addrs, const 
                               const kvx_launch *launch, void *stream);
 
 /* Non-blocking: if the piece in flight has completed, submit the next one.
- * *done = 1 once every piece has completed. */
+ * *done = 1 once every piece has completed. Start, poll and progress calls on
+ * one transfer from several threads take turns (the transfer holds a lock). */
 kvx_status kvx_transfer_poll(kvx_transfer *t, int *done);
 
 /* Descriptors submitted so far and in total (either pointer may be NULL). */

@@ -79,3 +79,43 @@ def test_transfer_owns_its_descriptors_and_refuses_overlap_in_time():
     finally:
         t.close()
         p.close()
+
+
+def test_one_transfer_polled_from_several_threads():
+    # Three threads poll the same transfer while the main thread reads its progress:
+    # the transfer's lock makes them take turns, so every piece is submitted once,
+    # after the previous one completed, and the bytes match the oracle.
+    import threading
+    w = W.kv_burst(n_sets=1, n_per_dir=16_384, pool_bytes=256 * W.MIB)
+    h2d = w.batches[0][0]
+    p = Pools(w.pools)
+    t = kvx.Transfer()
+    try:
+        want = p.expected([h2d])
+        s = torch.cuda.Stream()
+        t.start(*p.addrs(h2d), "h2d", 1000, stream=s)
+        errors, seen = [], []
+
+        def poller():
+            try:
+                t0 = time.perf_counter()
+                while not t.poll():
+                    assert time.perf_counter() - t0 < 30.0, "transfer did not finish"
+            except Exception as e:  # surfaced below
+                errors.append(repr(e))
+
+        ts = [threading.Thread(target=poller) for _ in range(3)]
+        for th in ts:
+            th.start()
+        while any(th.is_alive() for th in ts):
+            seen.append(t.progress()[0])
+        for th in ts:
+            th.join()
+        assert not errors, errors
+        assert t.progress() == (h2d.n, h2d.n)
+        assert seen == sorted(seen) and all(x % 1000 == 0 or x == h2d.n for x in seen)
+        kvx.kvx_stream_check(s)
+        p.assert_equal(want)
+    finally:
+        t.close()
+        p.close()
