@@ -596,14 +596,24 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // batch faster than 1,216: 4 KiB x 4,096 back to back 0.845 of HBM, 0.83 with
 // 304 x 256, 0.73-0.77 with 1,216 x 128. From 32 MiB up the 1,216-CTA row is
 // as fast or faster (8 KiB x 4,096: 0.895-0.909 against 0.885).
+//
+// Above 24 MiB the grid depends on the LDG instance. The phase-matched one
+// (84 registers a thread: 5 CTAs of 128 threads per SM) is faster with 1,824
+// CTAs than with 1,216 on every graded aligned cell, as a stream of batches
+// (4 KiB x 65,536: 0.943 -> 0.952, 8 KiB x 65,536: 0.944 -> 0.972, 12 KiB x
+// 4,096: 0.864 -> 0.944, 24 KiB x 21,845: 0.950 -> 0.962) and timed alone
+// (+0 to +1.3 points). The re-pairing one (118 registers: 4 CTAs per SM) is
+// not (odd-tail cells of 28-108 MiB: -1.8 to +2.0 points), so phase-mismatched
+// batches below the STAGE row keep 1,216 CTAs.
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 1216, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
-    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
+    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 
 int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
