@@ -589,6 +589,13 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 65,536 0.936 against 0.898, 16 KiB x 32,768 0.948 against 0.921, 28 KiB x
 // 18,724 0.942 against 0.920. Smaller ones stay with LDG (16 KiB x 4,096 odd:
 // 0.890 LDG against 0.856), as do matched batches (phase-matched LDG: 0.97-0.99).
+// More, smaller grids of warps serve STAGE better (two sweeps of stages x
+// CTAs, back to back and alone): with chunks longer than one 4 KiB unit, 4
+// stages and 3,648 CTAs (8 KiB to 28 KiB odd cells: 0.952-0.976 as a stream
+// and alone, against 0.921-0.941 and 0.940-0.952 with 1,216); with chunks of
+// one unit, so that each warp has only a few units, 2 stages and 2,432 CTAs
+// (4 KiB x 65,536 odd: 0.901 / 0.923 against 0.895 / 0.917; 4 stages lose
+// there as the grid grows, 0.756 at 7,296 CTAs).
 //
 // D2D batches of at most 24 MiB take one 512-thread CTA per SM: timed alone a
 // 16 MiB batch is launch-bound with any grid (0.49 of HBM), but as a stream
@@ -608,7 +615,8 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 1216, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
+    {KVX_D2D, 4096, {KVX_VARIANT_STAGE, 2432, 128, 8, 2, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 3648, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
     {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},

@@ -521,8 +521,10 @@ def test_select_launch_d2d_rows_follow_payload_and_alignment():
 def test_select_launch_stage_row_for_mismatched_phases():
     # D2D batches of 128 MiB or more with a chunk whose source and destination differ mod 16
     l = kvx.kvx_select_launch(*_batch(65536, 4096, slot=8192, src_phase=8), None, "d2d")
-    assert (l["variant"], l["threads"], l["unroll"], l["stages"]) == (kvx.KVX_VARIANT_STAGE, 128, 0, 4)
-    assert l["cta_budget"] == 1216 and l["assign"] == 0
+    assert (l["variant"], l["threads"], l["unroll"], l["stages"]) == (kvx.KVX_VARIANT_STAGE, 128, 0, 2)
+    assert l["cta_budget"] == 2432 and l["assign"] == 0  # chunks of one 4 KiB unit: 2 stages, 2,432 CTAs
+    l = kvx.kvx_select_launch(*_batch(32768, 8192, slot=16384, src_phase=8), None, "d2d")
+    assert (l["variant"], l["stages"], l["cta_budget"]) == (kvx.KVX_VARIANT_STAGE, 4, 3648)  # longer chunks
     # one mismatched chunk is enough; 16-byte phases that agree are not
     s, d, z = _batch(32768, 8192, slot=16384)
     assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
