@@ -609,16 +609,19 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // CTAs than with 1,216 on every graded aligned cell, as a stream of batches
 // (4 KiB x 65,536: 0.943 -> 0.952, 8 KiB x 65,536: 0.944 -> 0.972, 12 KiB x
 // 4,096: 0.864 -> 0.944, 24 KiB x 21,845: 0.950 -> 0.962) and timed alone
-// (+0 to +1.3 points). The re-pairing one (118 registers: 4 CTAs per SM) is
-// not (odd-tail cells of 28-108 MiB: -1.8 to +2.0 points), so phase-mismatched
-// batches below the STAGE row keep 1,216 CTAs.
+// (+0 to +1.3 points). Phase-mismatched D2D batches run the one-path
+// instance (kvx::kPhaseShift, 79 registers: 6 CTAs per SM) rather than the
+// re-pairing one (118 registers), also with 1,824 CTAs: against re-pairing
+// with 1,216, odd-tail cells of 28-108 MiB +1.0 to +4.0 points as a stream
+// (8 KiB x 4,096: 0.780 -> 0.820) and +0 to +2.8 alone, same box, alternating
+// builds.
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2D, 4096, {KVX_VARIANT_STAGE, 2432, 128, 8, 2, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 3648, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
     {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
@@ -721,6 +724,7 @@ kvx_status resolve(int dir, const BatchShape &shape, const kvx_launch *want, Lau
     out->store_policy = policy;
     out->assign = assign;
     out->matched = shape.matched;
+    out->shift = dir == KVX_D2D;  // see kvx::kPhaseShift
     out->pdl = e.pdl;
     out->prefetch = prefetch_for(dir, shape.payload);
     return KVX_OK;

@@ -44,8 +44,17 @@ struct Launch {
     int store_policy;  // LDG store cache policy
     int assign;        // LDG: KVX_ASSIGN_STATIC or KVX_ASSIGN_DYNAMIC
     bool matched;      // LDG: every chunk's src and dst agree mod 16 (decided from the packed batch)
+    bool shift;        // LDG, not matched: the one-path instance (kPhaseShift) instead of re-pairing
     bool pdl;          // launch with programmatic stream serialisation (KVX_PDL, default on)
     bool prefetch;     // LDG by position: prefetch the first units' sources into L2 before the wait
+};
+
+// The LDG kernel's instances (its template argument M), by how they copy a
+// chunk whose src and dst differ in phase mod 16.
+enum : int {
+    kPhaseRepair = 0,   // a phase-matched path and a re-pairing path, chosen per chunk
+    kPhaseMatched = 1,  // no such chunk in the batch (checked per record)
+    kPhaseShift = 2,    // one path for both phases (source words shifted by 0 or 8 bytes)
 };
 
 // LDG kernel flags.

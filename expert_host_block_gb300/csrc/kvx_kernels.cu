@@ -174,13 +174,23 @@ struct PassBytes {
     static constexpr uint32_t value = 512u * U;
 };
 
-// M: the caller guarantees that src and dst have the same phase mod 16, so the
-// re-pairing path is left out (82 instead of 118 registers a thread at U = 8).
-template <int U, int P, bool M = false>
+// M, the instance (kvx::kPhase*): kPhaseRepair takes the phase-matched path
+// below for chunks whose src and dst agree mod 16 and re-pairs 16-byte words
+// across lanes for the others (118 registers a thread at U = 8);
+// kPhaseMatched is called only for chunks that agree, so the re-pairing path
+// is left out (84 registers); kPhaseShift copies every chunk with one path
+// (copy_pass_shift, 79 registers).
+template <int U, int P, int M>
+__device__ __forceinline__ void copy_pass_shift(uint64_t s, uint64_t d, uint32_t len, uint32_t k,
+                                                uint32_t lane);
+
+template <int U, int P, int M = kPhaseRepair>
 __device__ __forceinline__ void copy_pass(uint64_t s, uint64_t d, uint32_t len, uint32_t k,
                                           uint32_t lane)
 {
-    if (M || ((s ^ d) & 15u) == 0) {
+    if constexpr (M == kPhaseShift) {
+        copy_pass_shift<U, P, M>(s, d, len, k, lane);
+    } else if (M == kPhaseMatched || ((s ^ d) & 15u) == 0) {
         const uint32_t head = (s & 15u) ? 8u : 0u;  // len >= 8 whenever head != 0
         const uint64_t bs = s + head, bd = d + head;
         const uint32_t blen = len - head;
@@ -220,7 +230,7 @@ __device__ __forceinline__ void copy_pass(uint64_t s, uint64_t d, uint32_t len, 
             if (idx < n16)
                 st16<P>(D + ((uint64_t)idx << 4), r[j]);
         }
-    } else if constexpr (!M) {
+    } else if constexpr (M == kPhaseRepair) {
         // Source and destination differ in phase mod 16 (one of them is 8 mod
         // 16). If the source is the 16-aligned one, its first 8 bytes go out as
         // a head word; after that the source is 8 mod 16 and the destination is
@@ -283,6 +293,77 @@ __device__ __forceinline__ void copy_pass(uint64_t s, uint64_t d, uint32_t len, 
             else if (idx == n16 && tail)
                 st8<P>(D + ((uint64_t)idx << 4), make_uint2(r[j].z, r[j].w));
         }
+    }
+}
+
+// Every chunk in the destination's frame: an 8-byte head when the destination
+// is 8 mod 16, aligned 16-byte destination words, an 8-byte tail. The aligned
+// 16-byte source words V[j] start `sh` bytes (0 or 8, the same for the whole
+// warp) before the source bytes of destination word j: with sh = 0 word j is
+// V[j], with sh = 8 it is the high half of V[j] and the low half of V[j + 1]
+// (re-paired across neighbouring lanes). One path for both phases needs no
+// more registers than the phase-matched instance; its grid is larger (it
+// fits 6 CTAs of 128 threads per SM, the re-pairing instance 4).
+template <int U, int P, int M>
+__device__ __forceinline__ void copy_pass_shift(uint64_t s, uint64_t d, uint32_t len, uint32_t k,
+                                                uint32_t lane)
+{
+    const uint32_t head = (d & 15u) ? 8u : 0u;  // len >= 8 whenever head != 0
+    const uint64_t bs = s + head;
+    const uint32_t sh = (uint32_t)(bs & 15u);   // 0 or 8
+    const uint32_t blen = len - head;
+    const uint32_t n16 = blen >> 4;              // whole destination words
+    const bool tail = (blen & 15u) != 0;         // then 8 bytes
+    // source words V[0 .. nv): with sh = 8 one more than the destination words
+    // (the low half of the last one, and the tail's high half)
+    const uint32_t nv = n16 + (((sh || tail) && (n16 || tail)) ? 1u : 0u);
+    // Each V[j] lies in a 16-byte block that holds source bytes, so no load
+    // leaves the pages of the source range; bytes outside it are never stored.
+    const unsigned char *V = reinterpret_cast<const unsigned char *>(bs - sh);
+    unsigned char *D = reinterpret_cast<unsigned char *>(d + head);
+    const bool edge = k == 0 && lane == 0 && head;  // the head word, pass 0
+    uint2 e = {0, 0};
+    if (edge)
+        e = ld8(reinterpret_cast<const unsigned char *>(s));
+    const uint32_t i0 = k * 32u * U;
+    uint4 r[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        const uint32_t idx = i0 + 32u * j + lane;
+        if (idx < nv)
+            r[j] = ld16(V + ((uint64_t)idx << 4));
+    }
+    uint2 x = {0, 0};  // sh = 8, lane 31: the low half of the word after this pass
+    const uint32_t ix = i0 + 32u * U;
+    if (sh && lane == 31 && ix < nv) {
+        const uint4 t = ld16(V + ((uint64_t)ix << 4));
+        x = make_uint2(t.x, t.y);
+    }
+    if (edge)
+        st8<P>(reinterpret_cast<unsigned char *>(d), e);
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        uint32_t nx = 0, ny = 0;
+        if (sh) {  // the same for every lane
+            nx = __shfl_down_sync(kFull, r[j].x, 1);
+            ny = __shfl_down_sync(kFull, r[j].y, 1);
+            if (j + 1 < U) {
+                const uint32_t fx = __shfl_sync(kFull, r[j + 1 < U ? j + 1 : j].x, 0);
+                const uint32_t fy = __shfl_sync(kFull, r[j + 1 < U ? j + 1 : j].y, 0);
+                if (lane == 31) {
+                    nx = fx;
+                    ny = fy;
+                }
+            } else if (lane == 31) {
+                nx = x.x;
+                ny = x.y;
+            }
+        }
+        const uint32_t idx = i0 + 32u * j + lane;
+        if (idx < n16)
+            st16<P>(D + ((uint64_t)idx << 4), sh ? make_uint4(r[j].z, r[j].w, nx, ny) : r[j]);
+        else if (idx == n16 && tail)
+            st8<P>(D + ((uint64_t)idx << 4), sh ? make_uint2(r[j].z, r[j].w) : make_uint2(r[j].x, r[j].y));
     }
 }
 
@@ -355,10 +436,10 @@ __device__ __forceinline__ Rec shfl_rec(const Rec &r, int src_lane)
 // agree mod 16; the host decides M from the same descriptors it packs, so a
 // mismatched record means a bad table: reported and skipped, never copied with
 // misaligned 16-byte accesses.
-template <bool M>
+template <int M>
 __device__ __forceinline__ bool phase_ok(const Rec &c, uint32_t lane, unsigned *err)
 {
-    if (!M || ((c.s ^ c.d) & 15u) == 0)
+    if (M != kPhaseMatched || ((c.s ^ c.d) & 15u) == 0)
         return true;
     if (lane == 0)
         report(err, kDevErrBadRecord);
@@ -381,7 +462,7 @@ __device__ __forceinline__ Rec unit_rec(const kvx_chunk *__restrict__ tab, uint6
 // every lane asks L2 for the source bytes of the unit whose record it holds,
 // so a batch launched early fetches its first data while the one before it
 // drains (4,096 x 8 KiB back to back: 0.83 -> 0.90 of HBM).
-template <int U, int P, bool M>
+template <int U, int P, int M>
 __global__ void __launch_bounds__(512) kvx_copy_ldg_kernel(const kvx_chunk *__restrict__ tab,
                                                             uint32_t n_chunks, uint32_t passes,
                                                             unsigned long long *ctr, unsigned *err,
@@ -1153,11 +1234,15 @@ cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), int ctas, int threads, 
 
 template <int U, int P>
 cudaError_t launch_ldg(bool pdl, int ctas, int threads, const kvx_chunk *t, uint32_t n, uint32_t passes,
-                       unsigned long long *ctr, bool matched, unsigned *err, uint32_t flags, cudaStream_t s)
+                       unsigned long long *ctr, int phase, unsigned *err, uint32_t flags, cudaStream_t s)
 {
-    if (matched)
-        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, true>, ctas, threads, 0, s, t, n, passes, ctr, err, flags);
-    return launch_k(pdl, kvx_copy_ldg_kernel<U, P, false>, ctas, threads, 0, s, t, n, passes, ctr, err, flags);
+    if (phase == kPhaseMatched)
+        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, kPhaseMatched>, ctas, threads, 0, s, t, n, passes, ctr, err,
+                        flags);
+    if (phase == kPhaseShift)
+        return launch_k(pdl, kvx_copy_ldg_kernel<U, P, kPhaseShift>, ctas, threads, 0, s, t, n, passes, ctr, err,
+                        flags);
+    return launch_k(pdl, kvx_copy_ldg_kernel<U, P, kPhaseRepair>, ctas, threads, 0, s, t, n, passes, ctr, err, flags);
 }
 
 template <int U>
@@ -1165,10 +1250,11 @@ cudaError_t launch_ldg_p(const Launch &l, int ctas, const kvx_chunk *t, uint32_t
                          uint32_t passes, unsigned long long *ctr, unsigned *err, cudaStream_t s)
 {
     const uint32_t flags = (l.prefetch && ctr == nullptr) ? kLdgPrefetch : 0u;
+    const int ph = l.matched ? kPhaseMatched : l.shift ? kPhaseShift : kPhaseRepair;
     switch (l.store_policy) {
-    case 1: return launch_ldg<U, 1>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
-    case 2: return launch_ldg<U, 2>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
-    default: return launch_ldg<U, 0>(l.pdl, ctas, l.threads, t, n, passes, ctr, l.matched, err, flags, s);
+    case 1: return launch_ldg<U, 1>(l.pdl, ctas, l.threads, t, n, passes, ctr, ph, err, flags, s);
+    case 2: return launch_ldg<U, 2>(l.pdl, ctas, l.threads, t, n, passes, ctr, ph, err, flags, s);
+    default: return launch_ldg<U, 0>(l.pdl, ctas, l.threads, t, n, passes, ctr, ph, err, flags, s);
     }
 }
 
