@@ -1145,7 +1145,7 @@ bool kvx::handle_live(const void *h, HandleKind kind)
 // descriptor buffers
 // ---------------------------------------------------------------------------
 struct kvx_desc_buf {
-    std::mutex mu;
+    mutable std::mutex mu;  // uploads, copies and info calls on one buffer take turns
     int device = 0;
     size_t cap = 0;
     kvx_chunk *dev = nullptr;   // header record, then the chunk records
@@ -1527,6 +1527,7 @@ kvx_status kvx_desc_buf_info(const kvx_desc_buf *b, size_t *n_chunks, uint64_t *
         return fail(KVX_ERR_INVALID_ARG, "null descriptor buffer");
     if (!kvx::handle_live(b, kvx::kHandleDescBuf))
         return fail(KVX_ERR_INVALID_ARG, "not a live descriptor buffer (destroyed, or never created)");
+    std::lock_guard<std::mutex> g(b->mu);
     if (n_chunks)
         *n_chunks = b->n_chunks;
     if (payload)
