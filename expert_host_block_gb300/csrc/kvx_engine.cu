@@ -611,17 +611,22 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 4,096: 0.864 -> 0.944, 24 KiB x 21,845: 0.950 -> 0.962) and timed alone
 // (+0 to +1.3 points). Phase-mismatched D2D batches run the one-path
 // instance (kvx::kPhaseShift, 79 registers: 6 CTAs per SM) rather than the
-// re-pairing one (118 registers), also with 1,824 CTAs: against re-pairing
-// with 1,216, odd-tail cells of 28-108 MiB +1.0 to +4.0 points as a stream
-// (8 KiB x 4,096: 0.780 -> 0.820) and +0 to +2.8 alone, same box, alternating
-// builds.
+// re-pairing one (118 registers): against re-pairing with 1,216 CTAs, with
+// 1,824 CTAs odd-tail cells of 28-108 MiB gained +1.0 to +4.0 points as a
+// stream (8 KiB x 4,096: 0.780 -> 0.820) and +0 to +2.8 alone (same box,
+// alternating builds). Its grid then follows the payload: up to 32 MiB 1,216
+// CTAs (8 KiB x 4,096 odd: 0.845 against 0.822 with 1,824), above it 3,040
+// (60 / 92 / 108 MiB odd: 0.864 / 0.886 / 0.904 as a stream and 0.922 /
+// 0.941 / 0.955 alone, against 0.843 / 0.868 / 0.885 and 0.883 / 0.889 /
+// 0.922 with 1,824; 44 MiB even as a stream, +2.8 points alone).
 const TableRow kTable[] = {
     {KVX_H2D, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2H, ~0ull, {KVX_VARIANT_LDG, 64, 256, 8, 3, 0, KVX_ASSIGN_DYNAMIC}},
     {KVX_D2D, 4096, {KVX_VARIANT_STAGE, 2432, 128, 8, 2, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_STAGE, 3648, 128, 8, 4, 0, KVX_ASSIGN_STATIC}, 128ull << 20, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true, 32ull << 20},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 3040, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
     {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
