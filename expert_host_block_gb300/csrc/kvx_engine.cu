@@ -604,12 +604,15 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 304 x 256, 0.73-0.77 with 1,216 x 128. From 32 MiB up the 1,216-CTA row is
 // as fast or faster (8 KiB x 4,096: 0.895-0.909 against 0.885).
 //
-// Above 24 MiB the grid depends on the LDG instance. The phase-matched one
-// (84 registers a thread: 5 CTAs of 128 threads per SM) is faster with 1,824
-// CTAs than with 1,216 on every graded aligned cell, as a stream of batches
-// (4 KiB x 65,536: 0.943 -> 0.952, 8 KiB x 65,536: 0.944 -> 0.972, 12 KiB x
-// 4,096: 0.864 -> 0.944, 24 KiB x 21,845: 0.950 -> 0.962) and timed alone
-// (+0 to +1.3 points). Phase-mismatched D2D batches run the one-path
+// Above 24 MiB the grid depends on the LDG instance and the payload. The
+// phase-matched one (84 registers a thread: 5 CTAs of 128 threads per SM) is
+// faster with 1,824 CTAs than with 1,216 on every graded aligned cell, as a
+// stream of batches (4 KiB x 65,536: 0.943 -> 0.952, 8 KiB x 65,536: 0.944 ->
+// 0.972, 12 KiB x 4,096: 0.864 -> 0.944, 24 KiB x 21,845: 0.950 -> 0.962) and
+// timed alone (+0 to +1.3 points); above 48 MiB 3,648 CTAs are faster still
+// on every cell (+1.1 points as a stream and +1.0 alone on average; 24 KiB x
+// 21,845: 0.960 / 0.976 -> 0.982 / 0.992), up to it 1,824 (12 KiB x 4,096:
+// 0.944 against 0.919). Phase-mismatched D2D batches run the one-path
 // instance (kvx::kPhaseShift, 79 registers: 6 CTAs per SM) rather than the
 // re-pairing one (118 registers): against re-pairing with 1,216 CTAs, with
 // 1,824 CTAs odd-tail cells of 28-108 MiB gained +1.0 to +4.0 points as a
@@ -627,9 +630,10 @@ const TableRow kTable[] = {
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 152, 512, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 24ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true, 32ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 3040, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
-    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 48ull << 20},
+    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 3648, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
     {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 3648, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 
 int default_assign(int dir) { return dir == KVX_D2D ? KVX_ASSIGN_STATIC : KVX_ASSIGN_DYNAMIC; }
@@ -1638,6 +1642,9 @@ kvx_status kvx_copy_device_list(kvx_devlist *l, const uint64_t *src, const uint6
         return fail(KVX_ERR_INVALID_ARG, "device lists are copied by the LDG variant only");
     BatchShape list_shape;
     list_shape.matched = true;  // not a STAGE row: the list's phases are not known on the host
+    // nor its payload, and the grid is not clamped to the work: take the
+    // mid-size rows rather than the largest batches' grids
+    list_shape.payload = 48ull << 20;
     kvx_launch merged = table_launch(dir, list_shape);
     if (want) {
         if (want->cta_budget < 0)

@@ -547,15 +547,17 @@ def test_select_launch_stage_row_for_mismatched_phases():
 
 def test_select_launch_small_d2d_row():
     # D2D batches of at most 24 MiB: one 512-thread CTA per SM; from just above it, 128-thread CTAs:
-    # 1,824 of them for phase-matched batches; for batches with a chunk whose phases differ (the
-    # one-path instance) 1,216 up to 32 MiB and 3,040 above, up to the STAGE row's 128 MiB
+    # for phase-matched batches 1,824 of them up to 48 MiB and 3,648 above; for batches with a chunk
+    # whose phases differ (the one-path instance) 1,216 up to 32 MiB and 3,040 above, up to the STAGE
+    # row's 128 MiB
     small = kvx.kvx_select_launch(*_batch(6144, 4096), None, "d2d")  # 24 MiB
     assert (small["variant"], small["threads"], small["unroll"]) == (kvx.KVX_VARIANT_LDG, 512, 8)
     assert small["cta_budget"] == 152  # 6,144 units need 384 CTAs of 16 warps: the budget binds
     assert kvx.kvx_select_launch(*_batch(1024, 4096), None, "d2d")["cta_budget"] == 64  # 1,024 units: the work binds
     big = kvx.kvx_select_launch(*_batch(6146, 4096), None, "d2d")
     assert (big["threads"], big["cta_budget"]) == (128, 1537)  # 6,146 units of 4 warps a CTA: the work binds
-    assert kvx.kvx_select_launch(*_batch(16384, 4096), None, "d2d")["cta_budget"] == 1824  # 64 MiB, matched
+    assert kvx.kvx_select_launch(*_batch(16384, 4096), None, "d2d")["cta_budget"] == 3648  # 64 MiB, matched
+    assert kvx.kvx_select_launch(*_batch(12288, 4096), None, "d2d")["cta_budget"] == 1824  # 48 MiB, matched
     odd = kvx.kvx_select_launch(*_batch(16384, 4096, slot=8192, src_phase=8), None, "d2d")  # 64 MiB, mismatched
     assert (odd["variant"], odd["threads"], odd["cta_budget"]) == (kvx.KVX_VARIANT_LDG, 128, 3040)
     odd = kvx.kvx_select_launch(*_batch(7168, 4096, slot=8192, src_phase=8), None, "d2d")  # 28 MiB, mismatched
