@@ -572,14 +572,15 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 16-28 KiB with 8-byte tails ran at 0.75 TB/s where LDG reaches 3.
 //
 // D2D, from the mean of 30 L2-flushed launches per shape (the event timer
-// ticks in ~1 us, so medians of short launches are coarse): the bulk ring is
-// fastest for batches of 256 MiB and more of full 16 KiB chunks (16 KiB x
-// 32,768: 0.992 of HBM with 456 CTAs and 96 KiB rings, against 0.985 for LDG;
-// 64 KiB x 8,192: 0.996 against 0.985), and LDG for everything else, with
-// 1,216 CTAs of 128 threads (about two waves of the SMs): 4 KiB x 65,536
-// 0.971, 24 KiB x 21,845 (chunks of 16 and 8 KiB, which waste the ring's
-// stages) 0.974 against 0.934 for the ring, 16 KiB x 4,096 0.981 against
-// 0.894 for the ring, whose fill and drain do not amortise over 64 MiB.
+// ticks in ~1 us, so medians of short launches are coarse), first calibrated
+// against LDG with 1,216 CTAs of 128 threads: the bulk ring was fastest for
+// batches of 256 MiB and more of full 16 KiB chunks (16 KiB x 32,768: 0.992
+// of HBM with 456 CTAs and 96 KiB rings, against 0.985; 64 KiB x 8,192: 0.996
+// against 0.985) and LDG for everything else (24 KiB x 21,845, chunks of 16
+// and 8 KiB that waste the ring's stages: 0.974 against 0.934 for the ring;
+// 16 KiB x 4,096: 0.981 against 0.894, the ring's fill and drain not
+// amortised over 64 MiB). The grids below were calibrated later, each shape
+// as a stream of batches and alone in the same process.
 //
 // D2D batches of 128 MiB and more with a chunk whose source and destination
 // differ mod 16 (the LDG kernel then runs its re-pairing instance, 118
@@ -612,7 +613,16 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // timed alone (+0 to +1.3 points); above 48 MiB 3,648 CTAs are faster still
 // on every cell (+1.1 points as a stream and +1.0 alone on average; 24 KiB x
 // 21,845: 0.960 / 0.976 -> 0.982 / 0.992), up to it 1,824 (12 KiB x 4,096:
-// 0.944 against 0.919). Phase-mismatched D2D batches run the one-path
+// 0.944 against 0.919). From 256 MiB up more CTAs still pay: with static
+// assignment a CTA's share of the work is fixed, and a grid many times what
+// fits at once lets the block scheduler start a new CTA wherever one has
+// finished. With 9,728 CTAs the 256-512 MiB aligned cells read 0.977-0.995 of
+// HBM as a stream and 0.992-1.004 alone, above the bulk ring that held this
+// class before (16 KiB x 32,768: 0.972 / 0.984 -> 0.992 / 0.998; 32 KiB x
+// 16,384: 0.955 / 0.982 -> 0.988 / 0.997 with 4,864; 64 KiB x 8,192: 0.947 /
+// 0.988 -> 0.991 / 0.997), so no built-in row picks the ring any more; it stays
+// for the tail policy (few one-warp CTAs beside a colocated kernel) and for
+// KVX_TABLE rows. Phase-mismatched D2D batches run the one-path
 // instance (kvx::kPhaseShift, 79 registers: 6 CTAs per SM) rather than the
 // re-pairing one (118 registers): against re-pairing with 1,216 CTAs, with
 // 1,824 CTAs odd-tail cells of 28-108 MiB gained +1.0 to +4.0 points as a
@@ -631,8 +641,7 @@ const TableRow kTable[] = {
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1216, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true, 32ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 3040, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, true},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 1824, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 0, false, 48ull << 20},
-    {KVX_D2D, 16383, {KVX_VARIANT_LDG, 3648, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
-    {KVX_D2D, ~0ull, {KVX_VARIANT_BULK, 456, 256, 8, 6, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
+    {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 9728, 128, 8, 3, 0, KVX_ASSIGN_STATIC}, 256ull << 20},
     {KVX_D2D, ~0ull, {KVX_VARIANT_LDG, 3648, 128, 8, 3, 0, KVX_ASSIGN_STATIC}},
 };
 

@@ -376,13 +376,14 @@ kvx_status kvx_select_launch(const uint64_t *src_addrs, const uint64_t *dst_addr
 
 /* The calibrated launch configuration for a direction and mean chunk size,
  * for a large batch of 16-byte aligned descriptors. Rows are chosen by
- * direction, mean chunk size and, for some rows, the batch's payload (the D2D
- * bulk row needs 256 MiB or more). A row that selects KVX_VARIANT_BULK applies
- * only to batches with at least 90 % of their bytes in descriptors whose
- * source, destination and size are multiples of 16; the D2D row that selects
- * KVX_VARIANT_STAGE only to batches of 128 MiB or more with a chunk whose
- * source and destination differ mod 16; other batches take the next matching
- * row. */
+ * direction, mean chunk size and, for some rows, the batch's payload and
+ * phases (the D2D grids grow with the payload; the D2D rows that select
+ * KVX_VARIANT_STAGE apply only to batches of 128 MiB or more with a chunk
+ * whose source and destination differ mod 16). A row that selects
+ * KVX_VARIANT_BULK (none of the built-in ones; a KVX_TABLE file may have
+ * them) applies only to batches with at least 90 % of their bytes in
+ * descriptors whose source, destination and size are multiples of 16. A batch
+ * a row does not apply to takes the next matching row. */
 kvx_status kvx_default_launch(int dir, uint64_t mean_chunk_bytes, kvx_launch *out);
 
 /* Process-wide validation level for kvx_copy_batch / kvx_upload_descriptors

@@ -368,12 +368,12 @@ def test_auto_path_rules():
     assert kvx.kvx_auto_path(s, d, np.full(17, M), None, "h2d", "tail") == "kernel_bulk"
     # two ranges with a mean below 2 x 256 KiB: kernel
     assert kvx.kvx_auto_path([1 << 30, 1 << 31], [1 << 40, 1 << 41], [256 << 10, 8], None, "h2d") == "kernel_ldg"
-    # throughput takes the calibrated table's kernel: the bulk ring for 256 MiB of aligned 16 KiB D2D chunks,
+    # throughput takes the calibrated table's kernel: LDG for 256 MiB of aligned 16 KiB D2D chunks,
     # STAGE for 256 MiB of D2D chunks whose phases differ; the tail policy keeps its 4 bulk CTAs
     s = (1 << 32) + 32768 * g.permutation(32768)[:16384].astype(np.uint64)
     d = (1 << 36) + 32768 * np.arange(16384, dtype=np.uint64)
     z = np.full(16384, 16384, dtype=np.uint64)
-    assert kvx.kvx_auto_path(s, d, z, None, "d2d") == "kernel_bulk"
+    assert kvx.kvx_auto_path(s, d, z, None, "d2d") == "kernel_ldg"
     assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "d2d") == "kernel_stage"
     assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "d2d", "tail") == "kernel_bulk"
     assert kvx.kvx_auto_path(s + np.uint64(8), d, z, None, "h2d") == "kernel_ldg"
@@ -491,24 +491,35 @@ def test_select_launch_kv_burst_and_tiny():
     assert kvx.kvx_select_launch([], [], [], None, "h2d")["cta_budget"] == 0
 
 
-def test_select_launch_d2d_rows_follow_payload_and_alignment():
-    # 16 KiB chunks: the bulk ring from 256 MiB up, when 16-byte aligned
+def test_select_launch_d2d_rows_follow_payload_and_alignment(tmp_path):
+    # phase-matched 16 KiB chunks: LDG with 9,728 CTAs from 256 MiB up, 3,648 below (above 48 MiB)
     big = kvx.kvx_select_launch(*_batch(16384, 16384), None, "d2d")
-    assert (big["variant"], big["cta_budget"], big["stages"], big["threads"]) == (kvx.KVX_VARIANT_BULK, 456, 6, 0)
+    assert (big["variant"], big["cta_budget"], big["threads"]) == (kvx.KVX_VARIANT_LDG, 9728, 128)
     below = kvx.kvx_select_launch(*_batch(16383, 16384), None, "d2d")
-    assert below["variant"] == kvx.KVX_VARIANT_LDG and below["threads"] == 128
-    # chunks of 16 and 8 KiB (mean 12 KiB) stay with LDG at any payload
-    assert kvx.kvx_select_launch(*_batch(16384, 24576), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    assert (below["variant"], below["cta_budget"], below["threads"]) == (kvx.KVX_VARIANT_LDG, 3648, 128)
+    # chunks of 16 and 8 KiB (mean 12 KiB) alike
+    assert kvx.kvx_select_launch(*_batch(16384, 24576), None, "d2d")["cta_budget"] == 9728
     odd = kvx.kvx_select_launch(*_batch(4096, 16384, slot=32768, src_phase=8), None, "d2d")
     assert odd["variant"] == kvx.KVX_VARIANT_LDG  # 64 MiB with phases that differ: below the STAGE row
-    # 9 % of the bytes misaligned (source and destination shifted alike) still takes the ring; 11 % does not
-    s, d, z = _batch(20000, 16384, slot=32768)
-    s[:1800] += 8
-    d[:1800] += 8
-    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_BULK
-    s[:2200] = s[:2200] | 8
-    d[:2200] = d[:2200] | 8
-    assert kvx.kvx_select_launch(s, d, z, None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
+    # a bulk row (from a table file) takes a batch with 9 % of its bytes misaligned (source and
+    # destination shifted alike), not one with 11 %
+    table = tmp_path / "t.txt"
+    table.write_text("d2d inf bulk 456 256 8 6 0 auto 268435456\n")
+    code = ("import sys, numpy as np\n"
+            "sys.path.insert(0, 'tests')\n"
+            "from test_abi_host import _batch\n"
+            "from expert_host_block_gb300 import kvx\n"
+            "s, d, z = _batch(20000, 16384, slot=32768)\n"
+            "s[:1800] += 8; d[:1800] += 8\n"
+            "a = kvx.kvx_select_launch(s, d, z, None, 'd2d')['variant']\n"
+            "s[:2200] = s[:2200] | 8; d[:2200] = d[:2200] | 8\n"
+            "b = kvx.kvx_select_launch(s, d, z, None, 'd2d')['variant']\n"
+            "print(a, b)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=root,
+                         env=dict(os.environ, KVX_TABLE=str(table)))
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(kvx.KVX_VARIANT_BULK), str(kvx.KVX_VARIANT_LDG)]
     # small chunks stay with LDG at any payload
     assert kvx.kvx_select_launch(*_batch(65536, 4096), None, "d2d")["variant"] == kvx.KVX_VARIANT_LDG
     # an explicit request wins over the table
@@ -590,7 +601,7 @@ def test_select_launch_with_table_file_payload_rows(tmp_path):
     out = _run_with_env(code, KVX_TABLE=str(table))
     lines = out.stdout.strip().splitlines()
     assert "'cta_budget': 77, 'threads': 128, 'unroll': 4" in lines[0], out.stderr
-    assert "'variant': 2, 'cta_budget': 456" in lines[1]  # 1 GiB: the file row does not apply
+    assert "'variant': 1, 'cta_budget': 9728" in lines[1]  # 1 GiB: the file row does not apply, the built-in one does
 
 
 def test_nvtx_switch_accepted():

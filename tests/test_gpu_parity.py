@@ -626,12 +626,12 @@ def test_status_token_pending_then_timeout_then_expiry():
     assert e.value.status == kvx.KVX_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("n,odd,variant", [(4096, False, "ldg"), (32768, False, "bulk"), (32768, True, "stage"),
+@pytest.mark.parametrize("n,odd,variant", [(4096, False, "ldg"), (32768, False, "ldg"), (32768, True, "stage"),
                                            (4096, True, "ldg")])
 def test_d2d_table_row_follows_shape(n, odd, variant):
-    # 16 KiB D2D chunks take the bulk row only for a batch of 256 MiB or more
-    # that is 16-byte aligned; with 8-byte phases that differ, a batch of 128 MiB
-    # or more takes the STAGE row (480 MiB here) and a smaller one LDG (60 MiB).
+    # 16 KiB D2D chunks take LDG when their phases agree (3,648 CTAs at 64 MiB,
+    # 9,728 at 512 MiB); with 8-byte phases that differ, a batch of 128 MiB or
+    # more takes the STAGE row (480 MiB here) and a smaller one LDG (60 MiB).
     w = W.sweep_cell(16, n, "d2d", odd_tails=odd)
     (b,) = w.batches
     p = Pools(w.pools)
