@@ -19,8 +19,8 @@
 //   - the copy engines occupy no SM at all, so the tail policy takes DMA
 //     whenever it stays near the link peak (at most 16 ranges of 1 MiB mean);
 //   - otherwise: the calibrated table's kernel for the batch (throughput:
-//     LDG over the host link, LDG, the bulk ring or STAGE for D2D by size,
-//     alignment and phase); the one-warp bulk CTAs at a budget of 4 cost the
+//     LDG over the host link, LDG or STAGE for D2D by size and phase, or the
+//     bulk ring where a KVX_TABLE file has a row for it); the one-warp bulk CTAs at a budget of 4 cost the
 //     colocated decode stand-in the least p99 while still sustaining a paced
 //     KV burst (tail).
 #include <cuda_runtime.h>

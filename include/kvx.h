@@ -329,7 +329,7 @@ kvx_status kvx_transfer_destroy(kvx_transfer *t);
  * kernel), for KVX_POLICY_TAIL at most 16 ranges averaging at least 1 MiB.
  * Everything else goes to the copy kernel: for THROUGHPUT the variant and
  * launch the calibrated table picks for the batch (kvx_select_launch with no
- * request: LDG, the bulk ring or STAGE), for TAIL the bulk variant with 4
+ * request: LDG or STAGE, or the bulk ring from a KVX_TABLE row), for TAIL the bulk variant with 4
  * one-warp CTAs (the lightest footprint beside a colocated decode). */
 typedef enum kvx_policy { KVX_POLICY_THROUGHPUT = 0, KVX_POLICY_TAIL = 1 } kvx_policy;
 typedef enum kvx_path {
