@@ -602,8 +602,8 @@ bool pack_fast(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, 
 // 16 MiB batch is launch-bound with any grid (0.49 of HBM), but as a stream
 // of batches (programmatic dependent launch) 152 CTAs hand over to the next
 // batch faster than 1,216: 4 KiB x 4,096 back to back 0.845 of HBM, 0.83 with
-// 304 x 256, 0.73-0.77 with 1,216 x 128. From 32 MiB up the 1,216-CTA row is
-// as fast or faster (8 KiB x 4,096: 0.895-0.909 against 0.885).
+// 304 x 256, 0.73-0.77 with 1,216 x 128. From 32 MiB up grids of 128-thread
+// CTAs are as fast or faster (8 KiB x 4,096: 0.895-0.909 against 0.885).
 //
 // Above 24 MiB the grid depends on the LDG instance and the payload. The
 // phase-matched one (84 registers a thread: 5 CTAs of 128 threads per SM) is
