@@ -60,6 +60,27 @@
  *     kvx_last_error() gives a one-line message for the calling thread.
  *     Device-side errors (a bounded wait that gave up) are reported by
  *     kvx_stream_check. No entry point aborts the process or traps the GPU.
+ *   - Environment (read once per process; an unknown or malformed value makes
+ *     every call fail with KVX_ERR_INVALID_ARG naming the variable, so a typo
+ *     never silently selects a default):
+ *       KVX_VARIANT=auto|ldg|bulk|stage   override the table's variant
+ *       KVX_CTA_BUDGET=<0..2^20>          override the table's grid budget (0: none)
+ *       KVX_VALIDATE=0|1|2                initial validation level
+ *       KVX_PDL=0|1                       programmatic dependent launch (1)
+ *       KVX_LOG=0|1|2                     stderr: failing statuses; + one line a batch
+ *       KVX_NVTX=0|1                      NVTX ranges around entry points and packing
+ *       KVX_PACK_THREADS=<0..64>          host packing threads for large batches
+ *       KVX_TABLE=<file>                  launch-table rows tried before the built-in
+ *         ones, one per line ('#' starts a comment):
+ *           dir max_mean_chunk variant cta_budget threads unroll stages
+ *               store_policy [assign [min_payload [phase [max_payload]]]]
+ *         dir h2d|d2h|d2d; max_mean_chunk and max_payload bytes or "inf";
+ *         variant ldg|bulk|stage; assign static|dynamic|auto; phase
+ *         any|unmatched (unmatched: only batches with a chunk whose source and
+ *         destination differ mod 16). A row applies when the batch's mean chunk
+ *         and payload fall within its bounds (a bulk row also needs 90 % of the
+ *         bytes in 16-byte aligned descriptors); explicit kvx_launch fields
+ *         override it.
  *   - Opaque handles (kvx_desc_buf, kvx_devlist, kvx_transfer): kvx keeps a
  *     registry of the live ones, so passing a destroyed handle, or a pointer
  *     that never was one, returns KVX_ERR_INVALID_ARG without touching it
