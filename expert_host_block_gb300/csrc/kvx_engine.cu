@@ -1597,8 +1597,7 @@ kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out)
         }
     }
     if (e == cudaSuccess)
-        e = cudaMalloc(reinterpret_cast<void **>(&l->meta),
-                       256 + ((size_t)max_n + 1) * sizeof(uint64_t));
+        e = cudaMalloc(reinterpret_cast<void **>(&l->meta), 256 + kvx::devlist_scratch_bytes(max_n));
     if (e == cudaSuccess)
         e = cudaEventCreateWithFlags(&l->last_use, cudaEventDisableTiming);
     if (e != cudaSuccess) {

@@ -28,8 +28,23 @@ struct DevListMeta {
     uint64_t total;      // chunks of the valid descriptors
     uint32_t n;          // descriptors taken (the count, clamped to the capacity)
     uint32_t max_chunk;  // longest chunk, bytes
-    unsigned long long next;  // the copy kernel's unit counter (zeroed by the plan kernel)
+    unsigned long long next;  // the copy kernel's unit counter (zeroed by the plan kernels)
+    uint32_t tiles;      // plan tiles of kListTile descriptors in use
 };
+
+// A device list's plan is computed in tiles of this many descriptors: each
+// descriptor's chunk offset within its tile, and per tile its first chunk
+// (tile base), longest chunk and error bits.
+constexpr uint32_t kListTile = 256;
+
+// Bytes of a device list's scratch after its 256-byte DevListMeta: (max_n + 1)
+// tile-relative chunk offsets, one 64-bit base and one 32-bit word (longest
+// chunk | error bits << 16) per tile.
+inline uint32_t devlist_tiles(uint32_t max_n) { return (max_n + kListTile - 1) / kListTile; }
+inline size_t devlist_scratch_bytes(uint32_t max_n)
+{
+    return ((size_t)max_n + 1) * 8 + (size_t)devlist_tiles(max_n) * 12 + 8;
+}
 
 // Bounded-wait limit of the bulk kernel's mbarrier waits (ns of %globaltimer).
 constexpr uint64_t kBulkWaitNs = 2000000000ull;

@@ -275,8 +275,10 @@ kvx_status kvx_desc_buf_destroy(kvx_desc_buf *buf);
  * fixed-shape and CUDA-graph capturable").
  *
  * A kvx_devlist holds the device scratch of such copies for lists of up to
- * max_n descriptors: 16 bytes of plan results and (max_n + 1) 64-bit chunk
- * offsets. Create it outside capture (it allocates device memory). */
+ * max_n descriptors: the plan results, each descriptor's 64-bit chunk offset
+ * within its tile of 256 descriptors, and 12 bytes per tile (its first chunk,
+ * longest chunk and error bits): about 8.05 bytes a descriptor. Create it
+ * outside capture (it allocates device memory). */
 typedef struct kvx_devlist kvx_devlist;
 
 kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out); /* 1 <= max_n <= 2^24 */
@@ -284,10 +286,12 @@ kvx_status kvx_devlist_destroy(kvx_devlist *list);                /* waits for i
 
 /* Enqueue the copy of the device-resident list: d_src, d_dst and d_sizes are
  * device arrays of at least max_n uint64 each (same meaning and rules as the
- * host arrays of kvx_copy_batch), d_count a device uint32 holding n. Two
- * launches on `stream`: a one-CTA plan kernel (validates, scans chunk
- * counts) and the LDG copy kernel with launch->cta_budget CTAs (the grid is
- * not clamped to the work, which the host does not know). No host work, no
+ * host arrays of kvx_copy_batch), d_count a device uint32 holding n. Three
+ * launches on `stream` (two for a list of at most 256 descriptors): the plan,
+ * as a tile kernel (up to 304 CTAs: validates tiles of 256 descriptors and
+ * scans their chunk counts) and a one-CTA kernel (scans the tile totals), then
+ * the LDG copy kernel with launch->cta_budget CTAs (the grid is not clamped to
+ * the work, which the host does not know). No host work, no
  * allocation, no synchronisation: allowed inside stream capture; replaying
  * the graph copies whatever the arrays and count hold at replay time.
  * Host-side errors (null or misaligned arrays, bad dir or launch, a BULK

@@ -237,3 +237,56 @@ def test_one_list_copied_from_two_streams():
     finally:
         lst.close()
         p.close()
+
+
+def test_list_of_more_than_4096_tiles():
+    # 1,100,000 descriptors: 4,297 plan tiles of 256, more than the copy kernel keeps in
+    # shared memory, so the tile bases are searched in global memory
+    n = 1_100_000
+    specs = {"src": W.PoolSpec("src", "device", 2 * n * 8, "random", (101,)),
+             "dst": W.PoolSpec("dst", "device", 2 * n * 8, "canary")}
+    p = Pools(specs)
+    lst = kvx.DeviceList(n)
+    arr = DevArrays(n)
+    try:
+        g = np.random.default_rng([W.SEED, 101])
+        so = (g.permutation(2 * n)[:n] * 8).astype(np.uint64)
+        do = (g.permutation(2 * n)[:n] * 8).astype(np.uint64)
+        sz = np.full(n, 8, dtype=np.uint64)
+        sz[g.random(n) < 0.01] = 0  # zero-size descriptors inside tiles
+        b = W.Batch("src", "dst", so, do, sz, "d2d")
+        want = p.expected([b])
+        arr.fill(*p.addrs(b))
+        lst.copy(*arr.ptrs(), "d2d")
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        lst.close()
+        p.close()
+
+
+def test_tiles_without_chunks_are_skipped():
+    # whole tiles of zero-size descriptors between tiles that copy: the tile search must land on
+    # the tile that holds each chunk, not on an empty one sharing its base
+    n = 256 * 12
+    specs = {"src": W.PoolSpec("src", "device", 4 * W.MIB, "random", (102,)),
+             "dst": W.PoolSpec("dst", "device", 4 * W.MIB, "canary")}
+    p = Pools(specs)
+    lst = kvx.DeviceList(n)
+    arr = DevArrays(n)
+    try:
+        g = np.random.default_rng([W.SEED, 102])
+        so = (g.permutation(4 * W.MIB // 1024)[:n] * 1024).astype(np.uint64)
+        do = (g.permutation(4 * W.MIB // 1024)[:n] * 1024).astype(np.uint64)
+        sz = (8 * g.integers(1, 129, n)).astype(np.uint64)
+        for t in (0, 3, 4, 7, 11):  # empty tiles, the first and the last among them
+            sz[t * 256:(t + 1) * 256] = 0
+        b = W.Batch("src", "dst", so, do, sz, "d2d")
+        want = p.expected([b])
+        arr.fill(*p.addrs(b))
+        lst.copy(*arr.ptrs(), "d2d")
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+    finally:
+        lst.close()
+        p.close()
