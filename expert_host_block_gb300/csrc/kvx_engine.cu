@@ -925,9 +925,11 @@ kvx_status ring_acquire(int dev, size_t chunks, Slot **out)
     return KVX_OK;
 }
 
-// Side streams of each device (one, for chunk-table uploads). Created on first
-// use with the device's highest priority, never destroyed.
-enum AuxKind { kAuxUpload = 0, kAuxKinds = 1 };
+// Side streams of each device (the chunk-table uploads of kvx_copy_batch, and
+// those of kvx_copy_batch_noalloc, which wait on the GPU for their table to be
+// free and must not hold up the others). Created on first use with the
+// device's highest priority, never destroyed.
+enum AuxKind { kAuxUpload = 0, kAuxNoalloc = 1, kAuxKinds = 2 };
 struct AuxStreams {
     std::mutex mu;
     cudaStream_t s[kAuxKinds] = {};
@@ -1935,27 +1937,119 @@ kvx_status kvx_selftest_wait_timeout(uint64_t timeout_ns, void *stream)
 // ---------------------------------------------------------------------------
 namespace {
 
-// The chunk table of kvx_copy_batch_noalloc (its header record, then up to
-// KVX_NOALLOC_MAX_CHUNKS records), in the library's own device memory: every
-// GPU that loads the library holds these 2 MiB until exit.
-static __device__ __align__(256) kvx_chunk g_noalloc_table[kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS];
+// The two chunk tables of kvx_copy_batch_noalloc (each its header record, then
+// up to KVX_NOALLOC_MAX_CHUNKS records, padded to 256 bytes), in the library's
+// own device memory: every GPU that loads the library holds these 4 MiB until
+// exit. Calls fill them in turn, so that one call's upload can run while the
+// previous call's copy still reads the other table; before an upload
+// overwrites a table, the GPU waits for the last copy that read it
+// (g_noalloc_read), on whichever stream that copy ran.
+constexpr size_t kNoallocRecords = (kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS + 7) / 8 * 8;
+static __device__ __align__(256) kvx_chunk g_noalloc_table[2][kNoallocRecords];
 
-// Host side of the table, same layout, header kept zero. It is packed here and
-// copied with a pageable cudaMemcpyAsync, which stages the bytes before it
-// returns, so the array can be refilled as soon as the call returns.
-kvx_chunk g_noalloc_stage[kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS];
+// Host side of the table, same layout, header kept zero. The first call
+// page-locks it (cudaHostRegister of the library's own static memory, as for
+// the error flags), so that each upload is one DMA straight from it: a
+// pageable copy went through the runtime's own staging buffer first and cost
+// a 16,384-chunk batch 7 % of its device time and 30 us of host time. The
+// next call packs only once the previous upload has completed (g_noalloc_up).
+// Should the registration fail, the copy stays pageable: the runtime then
+// stages the bytes before cudaMemcpyAsync returns, and no wait is needed.
+alignas(4096) kvx_chunk g_noalloc_stage[kvx::kTableHeader + KVX_NOALLOC_MAX_CHUNKS];
+bool g_noalloc_lock_tried = false;
+bool g_noalloc_locked = false;
+cudaEvent_t g_noalloc_up[kMaxDevices];  // per device: the last upload from the array
+int g_noalloc_up_dev = -1;              // device of an upload not yet waited for, or -1
+cudaEvent_t g_noalloc_read[kMaxDevices][2];  // per device and table: the last copy that read it
+unsigned g_noalloc_next[kMaxDevices];        // per device: the table the next call fills
 
 // Serialises callers from pack to launch: the host array has one owner at a
 // time, and calls on one stream enqueue upload and kernel back to back.
 std::mutex g_noalloc_mu;
 
-// Device address of g_noalloc_table per device. In host code the symbol is
+// Device addresses of the two tables per device. In host code the symbol is
 // only a host-side stand-in, so the address comes from cudaGetSymbolAddress
 // with the device current (first call on each device). The same first call
 // maps the library's error flags if no other call did (a registration of a
 // static host page, not an allocation).
-kvx_chunk *g_noalloc_dev[kMaxDevices];
+kvx_chunk *g_noalloc_dev[kMaxDevices][2];
 unsigned *g_noalloc_err[kMaxDevices];
+
+}  // namespace
+
+namespace {
+
+// With the lock held: the first call's setup on this device (the table's
+// device address, the error flags, the page-locked host array and its upload
+// event), then a wait until the previous upload no longer reads the array.
+kvx_status noalloc_prepare(int dev)
+{
+    if (!g_noalloc_dev[dev][0]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_table);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk tables)");
+        const kvx_status est = err_flags(dev, &g_noalloc_err[dev]);
+        if (est != KVX_OK)
+            return est;
+        for (int t = 0; t < 2; ++t)
+            if (!g_noalloc_read[dev][t])
+                KVX_CUDA_TRY(cudaEventCreateWithFlags(&g_noalloc_read[dev][t], cudaEventDisableTiming));
+        g_noalloc_dev[dev][0] = static_cast<kvx_chunk *>(p);
+        g_noalloc_dev[dev][1] = static_cast<kvx_chunk *>(p) + kNoallocRecords;
+    }
+    if (!g_noalloc_lock_tried) {
+        g_noalloc_lock_tried = true;
+        g_noalloc_locked = cudaHostRegister(g_noalloc_stage, sizeof(g_noalloc_stage), cudaHostRegisterPortable) ==
+                           cudaSuccess;
+        if (!g_noalloc_locked)
+            cudaGetLastError();  // keep the pageable copy
+    }
+    if (g_noalloc_locked && !g_noalloc_up[dev])
+        KVX_CUDA_TRY(cudaEventCreateWithFlags(&g_noalloc_up[dev], cudaEventDisableTiming));
+    if (g_noalloc_up_dev >= 0) {  // the array is still being read by the previous upload
+        KVX_CUDA_TRY(cudaEventSynchronize(g_noalloc_up[g_noalloc_up_dev]));
+        g_noalloc_up_dev = -1;
+    }
+    return KVX_OK;
+}
+
+// With the lock held and the array packed: upload it into the next table and
+// launch. The upload waits for the last copy that read that table. When
+// `stream` still has work queued, a page-locked upload goes on the side stream
+// and `stream` waits for it, so that it overlaps that work (as kvx_copy_batch's
+// uploads do); otherwise it goes on `stream`.
+kvx_status noalloc_launch(int dev, const kvx::Launch &l, uint64_t chunks, uint32_t max_chunk, cudaStream_t stream)
+{
+    const unsigned t = g_noalloc_next[dev];
+    kvx_chunk *table = g_noalloc_dev[dev][t];
+    cudaError_t qe = cudaSuccess;
+    const bool busy = stream_busy(stream, &qe);
+    if (qe != cudaSuccess)
+        return cuda_fail(qe, "cudaStreamQuery");
+    cudaStream_t up = stream;
+    if (busy && g_noalloc_locked)
+        KVX_CUDA_TRY(aux_stream(dev, kAuxNoalloc, &up));
+    KVX_CUDA_TRY(cudaStreamWaitEvent(up, g_noalloc_read[dev][t], 0));
+    KVX_CUDA_TRY(cudaMemcpyAsync(table, g_noalloc_stage, (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
+                                 cudaMemcpyHostToDevice, up));
+    g_noalloc_next[dev] = t ^ 1u;
+    if (g_noalloc_locked) {
+        KVX_CUDA_TRY(cudaEventRecord(g_noalloc_up[dev], up));
+        g_noalloc_up_dev = dev;
+        if (up != stream)
+            KVX_CUDA_TRY(cudaStreamWaitEvent(stream, g_noalloc_up[dev], 0));
+    }
+    cudaError_t e = kvx::launch_copy(l, table, (uint32_t)chunks, max_chunk, g_noalloc_err[dev], stream);
+    // Recorded whether or not the launch went in: `stream` is past the upload
+    // either way, and the next upload into this table waits for the event.
+    const cudaError_t re = cudaEventRecord(g_noalloc_read[dev][t], stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copy kernel launch");
+    if (re != cudaSuccess)
+        return cuda_fail(re, "cudaEventRecord(no-alloc table read)");
+    return KVX_OK;
+}
 
 }  // namespace
 
@@ -1969,6 +2063,33 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     kvx_status st = check_env();
     if (st != KVX_OK)
         return st;
+    kvx_launch want{};
+    want.cta_budget = cta_budget;
+    // The common batch (level-0 validation, every descriptor within one chunk)
+    // is validated while it is packed, in one pass split over the packing
+    // threads, as kvx_copy_batch does; anything else takes the exact path below.
+    if (validate_level() == 0 && n && n <= KVX_NOALLOC_MAX_CHUNKS && src && dst && sizes && dir >= KVX_H2D &&
+        dir <= KVX_D2D) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        int dev = -1;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess)
+            cudaGetLastError();  // the exact path below reports it
+        else if (cs == cudaStreamCaptureStatusNone && dev >= 0 && dev < kMaxDevices) {
+            std::lock_guard<std::mutex> g(g_noalloc_mu);
+            st = noalloc_prepare(dev);
+            if (st != KVX_OK)
+                return st;
+            uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
+            uint32_t max_chunk = 0;
+            Launch l;
+            if (pack_fast(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader, &chunks, &payload, &max_chunk,
+                          &aligned16, &phases) &&
+                payload && resolve(dir, batch_shape(chunks, payload, aligned16, phases), &want, &l) == KVX_OK) {
+                log_batch("kvx_copy_batch_noalloc", dir, n, chunks, payload, l);
+                return noalloc_launch(dev, l, chunks, max_chunk, stream);
+            }
+        }
+    }
     uint64_t chunks = 0, payload = 0, aligned16 = 0, phases = 0;
     uint32_t max_chunk = 0;
     st = validate(src, dst, sizes, n, dir, validate_level(), &chunks, &payload, &max_chunk, &aligned16, &phases);
@@ -1978,8 +2099,6 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
         return fail(KVX_ERR_CAPACITY,
                     "batch needs %llu chunks; kvx_copy_batch_noalloc holds at most KVX_NOALLOC_MAX_CHUNKS "
                     "(%u)", (unsigned long long)chunks, KVX_NOALLOC_MAX_CHUNKS);
-    kvx_launch want{};
-    want.cta_budget = cta_budget;
     Launch l;
     st = resolve(dir, batch_shape(chunks, payload, aligned16, phases), &want, &l);
     if (st != KVX_OK)
@@ -2000,22 +2119,10 @@ extern "C" kvx_status kvx_copy_batch_noalloc(const uint64_t *src, const uint64_t
     if (dev < 0 || dev >= kMaxDevices)
         return fail(KVX_ERR_INVALID_ARG, "device %d out of range", dev);
     std::lock_guard<std::mutex> g(g_noalloc_mu);
-    if (!g_noalloc_dev[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_table);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(no-alloc chunk table)");
-        const kvx_status est = err_flags(dev, &g_noalloc_err[dev]);
-        if (est != KVX_OK)
-            return est;
-        g_noalloc_dev[dev] = static_cast<kvx_chunk *>(p);
-    }
+    st = noalloc_prepare(dev);
+    if (st != KVX_OK)
+        return st;
     pack(src, dst, sizes, n, g_noalloc_stage + kvx::kTableHeader, chunks);
-    KVX_CUDA_TRY(cudaMemcpyAsync(g_noalloc_dev[dev], g_noalloc_stage,
-                                 (size_t)(chunks + kvx::kTableHeader) * sizeof(kvx_chunk),
-                                 cudaMemcpyHostToDevice, stream));
-    cudaError_t e = kvx::launch_copy(l, g_noalloc_dev[dev], (uint32_t)chunks, max_chunk, g_noalloc_err[dev], stream);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "copy kernel launch");
-    return KVX_OK;
+    log_batch("kvx_copy_batch_noalloc", dir, n, chunks, payload, l);
+    return noalloc_launch(dev, l, chunks, max_chunk, stream);
 }

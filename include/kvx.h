@@ -516,28 +516,38 @@ kvx_status kvx_copy_contiguous(uint64_t dst, uint64_t src, uint64_t bytes, int d
  * cudaHostRegister of new memory. (Host heap use is not excluded: validation
  * levels 1 and 2 sort a heap copy of the ranges, and the first pack of 32 Ki
  * records or more may start the library's packing threads.) Its chunk
- * table lives in a fixed array of KVX_NOALLOC_MAX_CHUNKS records (2 MiB) in the
- * library's own device memory, which every GPU that loads the library holds
- * until the process exits; the records are packed into a fixed host array of
- * the same size and copied with one cudaMemcpyAsync from that (pageable)
- * array, which the runtime stages before returning.
+ * table lives in one of two fixed arrays of KVX_NOALLOC_MAX_CHUNKS records
+ * (2 MiB each) in the library's own device memory, which every GPU that loads
+ * the library holds until the process exits; the records are packed into a
+ * fixed host array of the same size and copied with one cudaMemcpyAsync from
+ * that array into the two device arrays in turn.
  *   - A batch that needs more than KVX_NOALLOC_MAX_CHUNKS chunks returns
  *     KVX_ERR_CAPACITY and enqueues nothing.
  *   - Not allowed while `stream` is being captured (KVX_ERR_CAPTURE): the
  *     table upload reads the shared host array, which a replayed graph would
  *     read again with whatever another call had packed there since. Capture
  *     kvx_copy_uploaded over a kvx_desc_buf instead.
- *   - The first call on a device looks up the device address of the array
- *     (cudaGetSymbolAddress) with that device current and, unless another
- *     kvx call did, registers the library's static page of error flags with
- *     the driver (cudaHostRegister of existing memory, not an allocation).
- *   - Every call shares the one array per device. Calls from several host
- *     threads are serialised until their copy is enqueued, so calls on one
- *     stream are safe; calls on different streams whose copies overlap on the
- *     GPU race on the array and may copy wrong bytes. Order them (one stream,
- *     or events) when they may overlap.
- *   - Nothing in the array has to start at zero: each call writes every record
- *     its kernel reads, and the header record that holds the work counter. */
+ *   - The first call on a device looks up the device address of the arrays
+ *     (cudaGetSymbolAddress) with that device current, creates three events
+ *     and, unless another kvx call did, registers the library's static page
+ *     of error flags with the driver (cudaHostRegister of existing memory,
+ *     not an allocation). The first call in the process also page-locks the
+ *     static host array the same way, so that the upload is one DMA from it;
+ *     a later call then waits on the host until the previous call's upload
+ *     has completed before it packs the array again. If the array cannot be
+ *     page-locked, the upload is a pageable copy, which the runtime stages
+ *     before returning.
+ *   - Each upload into a device array first waits, on the GPU, for the last
+ *     copy that read that array, on whatever stream it ran. When `stream`
+ *     still has work queued, a page-locked upload runs on a side stream of
+ *     the library (created by the first such call on the device) and
+ *     `stream` waits for it, so that it overlaps that work; otherwise it runs
+ *     on `stream`. Calls from several host threads are serialised until
+ *     their copy is enqueued; calls on one stream or on different streams
+ *     are both safe.
+ *   - Nothing in the arrays has to start at zero: each call writes every
+ *     record its kernel reads, and the header record that holds the work
+ *     counter. */
 #define KVX_NOALLOC_MAX_CHUNKS 65536u
 
 kvx_status kvx_copy_batch_noalloc(const uint64_t *src_addrs, const uint64_t *dst_addrs,

@@ -5,8 +5,8 @@ that reserves nearly all HBM for its KV cache at start-up makes any later
 cudaMalloc fail, and a decode loop with a fixed per-step time budget cannot
 absorb an allocation, or the device-wide synchronisation of a cudaFree, in the
 middle of a step. kvx_copy_batch allocates its staging ring lazily, so those
-callers use kvx_copy_batch_noalloc, whose chunk table is a fixed 2 MiB array
-in the library's own device memory.
+callers use kvx_copy_batch_noalloc, whose chunk tables are two fixed 2 MiB
+arrays in the library's own device memory, filled in turn.
 
 What is checked: the same two batches (a KV-style 4 KiB batch, then an odd-tail
 batch that needs fewer chunks, so the second call runs over a table still
@@ -15,6 +15,9 @@ destination pool and once through kvx_copy_batch_noalloc into an identical
 pool; the two pools must match byte for byte (the bit-exact tolerance of every
 copy test here), and both must match the oracle. A batch one chunk too large
 is refused before anything is enqueued, and so is a call during stream capture.
+Calls alternating between two busy streams, so that each upload runs on the
+side stream while copies on both streams still read the tables, match the
+oracle too.
 
 This file sorts last so that a run stopping at its first failure has run every
 other test first; it also passes alone in a fresh process.
@@ -116,5 +119,34 @@ def test_noalloc_refused_inside_capture():
         kvx.kvx_stream_check(None)
         assert float(x[0]) == 1.0                 # the capture itself went on
         assert np.array_equal(p.snapshot("dst"), before)   # and enqueued no copy
+    finally:
+        p.close()
+
+
+def test_noalloc_calls_on_two_busy_streams():
+    # Twelve H2D batches (disjoint device slots) alternate between two streams.
+    # Each stream is kept busy (a 64 MiB device fill queued before every call),
+    # so the uploads take the side stream and overlap copies still running on
+    # both streams; each upload must wait for the last copy that read its table.
+    # A batch copied over another batch's records would leave its own slots at
+    # the canary and write the other's twice.
+    kv = W.kv_burst(n_sets=12, n_per_dir=2048, pool_bytes=256 * W.MIB)
+    batches = [W.Batch("src", "dst", b.src_off, b.dst_off, b.sizes, "h2d") for b, _ in kv.batches]
+    body = 256 * W.MIB
+    p = Pools({"src": W.PoolSpec("src", "host", body, "random", (80,)),
+               "dst": W.PoolSpec("dst", "device", body, "canary")})
+    try:
+        want = p.expected(batches)
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        filler = [torch.empty(64 * W.MIB, dtype=torch.uint8, device="cuda") for _ in streams]
+        torch.cuda.synchronize()
+        for i, b in enumerate(batches):
+            k = i % 2
+            with torch.cuda.stream(streams[k]):
+                filler[k].fill_(i)
+                kvx.kvx_copy_batch_noalloc(*p.addrs(b), None, "h2d", 0, streams[k])
+        torch.cuda.synchronize()
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
     finally:
         p.close()
