@@ -281,7 +281,11 @@ struct Range {
 kvx_status check_overlap(const uint64_t *src, const uint64_t *dst, const uint64_t *sizes, size_t n)
 {
     std::vector<Range> d;
-    d.reserve(n);
+    try {
+        d.reserve(n);
+    } catch (const std::exception &) {  // bad_alloc, or length_error past max_size
+        return fail(KVX_ERR_CAPACITY, "out of host memory for the overlap check of %zu descriptors", n);
+    }
     for (size_t i = 0; i < n; ++i)
         if (sizes[i])
             d.push_back({dst[i], dst[i] + sizes[i]});
@@ -1138,10 +1142,15 @@ std::mutex g_handles_mu;
 std::unordered_map<const void *, int> g_handles;  // live handle -> its kvx::HandleKind
 }  // namespace
 
-void kvx::handle_add(const void *h, HandleKind kind)
+bool kvx::handle_add(const void *h, HandleKind kind)
 {
     std::lock_guard<std::mutex> g(g_handles_mu);
-    g_handles[h] = kind;
+    try {
+        g_handles[h] = kind;
+    } catch (const std::bad_alloc &) {
+        return false;
+    }
+    return true;
 }
 
 bool kvx::handle_remove(const void *h, HandleKind kind)
@@ -1399,7 +1408,14 @@ kvx_status kvx_desc_buf_create(size_t max_chunks, kvx_desc_buf **out)
         return cuda_fail(e, "kvx_desc_buf_create");
     }
     b->cap = max_chunks;
-    kvx::handle_add(b, kvx::kHandleDescBuf);
+    if (!kvx::handle_add(b, kvx::kHandleDescBuf)) {
+        cudaFree(b->dev);
+        cudaFreeHost(b->host);
+        cudaEventDestroy(b->upload_done);
+        cudaEventDestroy(b->last_use);
+        delete b;
+        return fail(KVX_ERR_CAPACITY, "kvx_desc_buf_create: out of host memory");
+    }
     *out = b;
     return KVX_OK;
 }
@@ -1609,7 +1625,12 @@ kvx_status kvx_devlist_create(uint32_t max_n, kvx_devlist **out)
         return cuda_fail(e, "kvx_devlist_create");
     }
     l->offsets = reinterpret_cast<uint64_t *>(reinterpret_cast<char *>(l->meta) + 256);
-    kvx::handle_add(l, kvx::kHandleDevList);
+    if (!kvx::handle_add(l, kvx::kHandleDevList)) {
+        cudaFree(l->meta);
+        cudaEventDestroy(l->last_use);
+        delete l;
+        return fail(KVX_ERR_CAPACITY, "kvx_devlist_create: out of host memory");
+    }
     *out = l;
     return KVX_OK;
 }
@@ -2035,10 +2056,19 @@ kvx_status noalloc_launch(int dev, const kvx::Launch &l, uint64_t chunks, uint32
                                  cudaMemcpyHostToDevice, up));
     g_noalloc_next[dev] = t ^ 1u;
     if (g_noalloc_locked) {
-        KVX_CUDA_TRY(cudaEventRecord(g_noalloc_up[dev], up));
-        g_noalloc_up_dev = dev;
-        if (up != stream)
-            KVX_CUDA_TRY(cudaStreamWaitEvent(stream, g_noalloc_up[dev], 0));
+        cudaError_t ue = cudaEventRecord(g_noalloc_up[dev], up);
+        if (ue == cudaSuccess) {
+            g_noalloc_up_dev = dev;
+            if (up != stream)
+                ue = cudaStreamWaitEvent(stream, g_noalloc_up[dev], 0);
+        }
+        if (ue != cudaSuccess) {
+            // No later call could wait for this upload: finish it here, so that
+            // it neither reads the host array nor writes the table afterwards.
+            cudaStreamSynchronize(up);
+            g_noalloc_up_dev = -1;
+            return cuda_fail(ue, "no-alloc table upload ordering");
+        }
     }
     cudaError_t e = kvx::launch_copy(l, table, (uint32_t)chunks, max_chunk, g_noalloc_err[dev], stream);
     // Recorded whether or not the launch went in: `stream` is past the upload

@@ -123,7 +123,7 @@ kvx_status set_error(kvx_status status, const char *message);
 // free. (Destroying a handle while another thread still uses it remains the
 // caller's error.)
 enum HandleKind : int { kHandleDescBuf = 1, kHandleDevList = 2, kHandleTransfer = 3 };
-void handle_add(const void *h, HandleKind kind);
+bool handle_add(const void *h, HandleKind kind);     // false: out of host memory
 bool handle_remove(const void *h, HandleKind kind);  // false: not a live handle of that kind
 bool handle_live(const void *h, HandleKind kind);
 

@@ -61,7 +61,10 @@ kvx_status kvx_transfer_create(kvx_transfer **out)
     kvx_transfer *t = new (std::nothrow) kvx_transfer;
     if (!t)
         return kvx::set_error(KVX_ERR_CAPACITY, "kvx_transfer_create: out of host memory");
-    kvx::handle_add(t, kvx::kHandleTransfer);
+    if (!kvx::handle_add(t, kvx::kHandleTransfer)) {
+        delete t;
+        return kvx::set_error(KVX_ERR_CAPACITY, "kvx_transfer_create: out of host memory");
+    }
     *out = t;
     return KVX_OK;
 }
@@ -81,24 +84,34 @@ kvx_status kvx_transfer_start(kvx_transfer *t, const uint64_t *src, const uint64
     kvx_status st = kvx_validate(src, dst, sizes, n, dir, kvx_get_validate_level());
     if (st != KVX_OK)
         return st;
-    t->n = n;
+    // Nothing of the previous transfer is in flight: start from an empty one,
+    // so that a failure below leaves a transfer with nothing to submit.
+    t->n = 0;
     t->next = 0;
-    t->piece = chunk_descriptors ? chunk_descriptors : (n ? n : 1);
+    if (n == 0)
+        return KVX_OK;
+    try {
+        t->src.assign(src, src + n);
+        t->dst.assign(dst, dst + n);
+        t->sizes.assign(sizes, sizes + n);
+    } catch (const std::bad_alloc &) {
+        return kvx::set_error(KVX_ERR_CAPACITY, "kvx_transfer_start: out of host memory for the descriptors");
+    }
+    if (!t->done_ev) {
+        if (cudaGetDevice(&t->device) != cudaSuccess ||
+            cudaEventCreateWithFlags(&t->done_ev, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            t->done_ev = nullptr;
+            return kvx::set_error(KVX_ERR_CUDA, "kvx_transfer_start: cannot create its event");
+        }
+    }
+    t->n = n;
+    t->piece = chunk_descriptors ? chunk_descriptors : n;
     t->dir = dir;
     t->has_launch = launch != nullptr;
     if (launch)
         t->launch = *launch;
     t->stream = static_cast<cudaStream_t>(stream);
-    if (n == 0)
-        return KVX_OK;
-    t->src.assign(src, src + n);
-    t->dst.assign(dst, dst + n);
-    t->sizes.assign(sizes, sizes + n);
-    if (!t->done_ev) {
-        if (cudaGetDevice(&t->device) != cudaSuccess ||
-            cudaEventCreateWithFlags(&t->done_ev, cudaEventDisableTiming) != cudaSuccess)
-            return kvx::set_error(KVX_ERR_CUDA, "kvx_transfer_start: cannot create its event");
-    }
     return submit_piece(t);
 }
 

@@ -13,6 +13,7 @@
 #include <condition_variable>
 #include <cstdlib>
 #include <cstring>
+#include <exception>
 #include <mutex>
 #include <thread>
 #include <vector>
@@ -88,8 +89,14 @@ class Workers {
             if (end != v && !*end && x >= 0 && x <= 64)
                 n = (int)x;
         }
-        for (int i = 0; i < n; ++i)
-            pool_.emplace_back([this] { loop(); });
+        // A thread that cannot be started (resource limits) leaves the pool
+        // smaller, down to none: packing then runs on the caller's thread.
+        try {
+            pool_.reserve(n);
+            for (int i = 0; i < n; ++i)
+                pool_.emplace_back([this] { loop(); });
+        } catch (const std::exception &) {
+        }
     }
 
     // Take parts of job `g` until none is left; a worker that wakes after its
