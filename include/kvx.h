@@ -138,7 +138,8 @@ typedef enum kvx_status {
     KVX_ERR_INVALID_ARG = 1,  /* null array, bad dir/variant/budget, null address, address overflow */
     KVX_ERR_ALIGN = 2,        /* an address or size is not a multiple of 8 */
     KVX_ERR_OVERLAP = 3,      /* (validation level >= 1) destination ranges overlap */
-    KVX_ERR_CAPACITY = 4,     /* more than KVX_MAX_CHUNKS chunks, or more than a buffer holds */
+    KVX_ERR_CAPACITY = 4,     /* more than KVX_MAX_CHUNKS chunks, or more than a buffer holds, or the
+                                 host heap ran out (no C++ exception ever crosses this boundary) */
     KVX_ERR_NOT_MAPPED = 5,   /* (validation level 2) an address is not of the kind dir names */
     KVX_ERR_CUDA = 6,         /* a CUDA runtime call failed; see kvx_last_error() */
     KVX_ERR_TIMEOUT = 7,      /* a bounded device wait gave up (reported by kvx_stream_check) */
