@@ -17,7 +17,9 @@ copy test here), and both must match the oracle. A batch one chunk too large
 is refused before anything is enqueued, and so is a call during stream capture.
 Calls alternating between two busy streams, so that each upload runs on the
 side stream while copies on both streams still read the tables, match the
-oracle too.
+oracle too. At each validation level (0: the fused validate-and-pack pass;
+1 and 2: the two-pass path) a valid batch is exact, and a misaligned size or
+overlapping destinations are refused with nothing enqueued.
 
 This file sorts last so that a run stopping at its first failure has run every
 other test first; it also passes alone in a fresh process.
@@ -149,4 +151,44 @@ def test_noalloc_calls_on_two_busy_streams():
         kvx.kvx_stream_check(None)
         p.assert_equal(want)
     finally:
+        p.close()
+
+
+@pytest.mark.parametrize("level", [0, 1, 2])
+def test_noalloc_validation_levels_and_errors(level):
+    # Level 0 takes the fused validate-and-pack pass; levels 1 and 2 the exact
+    # two-pass path. Each level copies a valid 4 KiB D2D batch bit-exactly, and
+    # refuses, with nothing enqueued, a misaligned size (every level) and
+    # overlapping destinations (levels 1 and 2).
+    p = Pools({"src": W.PoolSpec("src", "device", 8 * W.MIB, "random", (81,)),
+               "dst": W.PoolSpec("dst", "device", 8 * W.MIB, "canary")})
+    old = kvx.kvx_get_validate_level()
+    try:
+        kvx.kvx_set_validate_level(level)
+        g = np.random.default_rng([W.SEED, 81, level])
+        n = 1024
+        so = (g.permutation(2048)[:n] * 4096).astype(np.uint64)
+        do = (g.permutation(2048)[:n] * 4096).astype(np.uint64)
+        b = W.Batch("src", "dst", so, do, np.full(n, 4096, dtype=np.uint64), "d2d")
+        want = p.expected([b])
+        kvx.kvx_copy_batch_noalloc(*p.addrs(b), None, "d2d", 0, None)
+        kvx.kvx_stream_check(None)
+        p.assert_equal(want)
+        before = {name: p.snapshot(name) for name in p.specs}
+        s, d, z = p.addrs(b)
+        z_bad = z.copy()
+        z_bad[n // 2] = np.uint64(4092)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_copy_batch_noalloc(s, d, z_bad, None, "d2d", 0, None)
+        assert e.value.status == kvx.KVX_ERR_ALIGN
+        if level >= 1:
+            d_ovl = d.copy()
+            d_ovl[n - 1] = d_ovl[0] + np.uint64(8)
+            with pytest.raises(kvx.KvxError) as e:
+                kvx.kvx_copy_batch_noalloc(s, d_ovl, z, None, "d2d", 0, None)
+            assert e.value.status == kvx.KVX_ERR_OVERLAP
+        kvx.kvx_stream_check(None)
+        p.assert_equal(before)
+    finally:
+        kvx.kvx_set_validate_level(old)
         p.close()
