@@ -1996,10 +1996,6 @@ std::mutex g_noalloc_mu;
 kvx_chunk *g_noalloc_dev[kMaxDevices][2];
 unsigned *g_noalloc_err[kMaxDevices];
 
-}  // namespace
-
-namespace {
-
 // With the lock held: the first call's setup on this device (the table's
 // device address, the error flags, the page-locked host array and its upload
 // event), then a wait until the previous upload no longer reads the array.
