@@ -597,10 +597,11 @@ KVX_NOALLOC_MAX_CHUNKS = 65536
 
 
 def kvx_copy_batch_noalloc(src_addrs, dst_addrs, sizes, n=None, dir=KVX_H2D, cta_budget=0, stream=None) -> None:
-    """kvx_copy_batch for callers that cannot allocate at copy time (fixed 2 MiB device table).
+    """kvx_copy_batch for callers that cannot allocate at copy time (two fixed 2 MiB device tables).
 
-    At most KVX_NOALLOC_MAX_CHUNKS chunks per call; calls on different streams
-    that overlap on the GPU share the table and race (see include/kvx.h).
+    At most KVX_NOALLOC_MAX_CHUNKS chunks per call; not allowed during stream
+    capture. Calls on one stream or on several are ordered by the library: each
+    upload waits for the last copy that read its table (see include/kvx.h).
     """
     s, d, z, n = _triple(src_addrs, dst_addrs, sizes, n)
     _check(_load().kvx_copy_batch_noalloc(s.ctypes.data, d.ctypes.data, z.ctypes.data, n, _dir(dir),
